@@ -1,0 +1,524 @@
+"""Benchmark of the NVFP4 four-over-six quantizer on GB300.
+
+Workload (one step): the activation batch of four 8192 x 4096 bf16 tensors,
+one per input family (F1 N(0,1), F2 with 0.1 % x100 outliers, F3 U(-1,1),
+F4 with 25 % zero / tiny blocks), each quantized four-over-six with 1x16
+blocks, a per-tensor FP32 amax computed on the device, E4M3 bound 448 and
+MSE with exact-FP32 candidate error.  A step runs the amax pass of all four
+tensors, then the encode of all four, so the encode reads its input from HBM
+(the four inputs total 256 MiB, twice the L2).
+
+`value` is whole-job HBM throughput in GB/s counting the algorithmic bytes
+once per tensor (read 2 B + write 0.5 B codes + 1/16 B scale per element);
+the amax pass's second read of x is not counted, so the figure is strict.
+`roofline` is the encode kernel alone (average launch inside the timed
+region).  `e2e` repeats the step through the same C-ABI calls starting from
+pinned host buffers, with the host->device copy of the inputs and the
+device->host copy of codes and scales inside the timed region.
+
+--impl reference times the CPU oracle (the reference for this path) on a
+bounded sample of the same workload.
+"""
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+ROWS, COLS = 8192, 4096
+ELEMS = ROWS * COLS
+BYTES_PER_ELEM = 2 + 0.5 + 1.0 / 16          # bf16 read, codes and scales written
+ALG_BYTES = int(ELEMS * BYTES_PER_ELEM)       # 85,983,232 per tensor
+METRIC = "4over6 quantize HBM GB/s (% of GB300 peak) and elements/s, 8192x4096 bf16"
+WORKLOAD = ("activation quantize 8192x4096 bf16, batch of 4 families (F1-F4), 1x16 blocks, "
+            "per-tensor amax computed on device, 4over6 MSE exact-FP32, E4M3 448")
+PROFILE = os.path.join(ROOT, "profiles", "quant1x16_activation_8192x4096.md")
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "nvfp4_quantization_precision_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode())
+                h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def _profiled_traffic():
+    """DRAM bytes per encode launch from the committed ncu summary, if it was
+    taken on the current kernel sources; None otherwise."""
+    try:
+        txt = open(PROFILE).read()
+    except OSError:
+        return None
+    m_hash = re.search(r"kernel_source_hash:\s*([0-9a-f]+)", txt)
+    m_tr = re.search(r"traffic_bytes_per_launch:\s*([0-9]+)", txt)
+    if not (m_hash and m_tr) or m_hash.group(1) != kernel_source_hash():
+        return None
+    return int(m_tr.group(1))
+
+
+# ----------------------------------------------------------------- clocks
+class ClockSampler:
+    """Reads the SM clock, power and clock-event reasons of one GPU every
+    5 ms through NVML (read-only queries) while the benchmark runs."""
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, uuid=None, index=0, period=0.005):
+        import ctypes
+        self.samples = []
+        self.max_mhz = None
+        self.ok = False
+        self._stop = threading.Event()
+        try:
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                return
+            h = ctypes.c_void_p()
+            rc = 1
+            if uuid:
+                rc = nv.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(h))
+            if rc != 0:
+                rc = nv.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(index), ctypes.byref(h))
+            if rc != 0:
+                return
+            self.nv, self.h = nv, h
+            mx = ctypes.c_uint()
+            if nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:
+                self.max_mhz = float(mx.value)
+            self._reasons_fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                getattr(nv, "nvmlDeviceGetCurrentClocksThrottleReasons")
+            self.ok = True
+            self.t = threading.Thread(target=self._run, args=(period,), daemon=True)
+            self.t.start()
+        except Exception:
+            self.ok = False
+
+    def _run(self, period):
+        import ctypes
+        clk, pw, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        while not self._stop.is_set():
+            t = time.time()
+            a = self.nv.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(clk))
+            b = self.nv.nvmlDeviceGetPowerUsage(self.h, ctypes.byref(pw))
+            c = self._reasons_fn(self.h, ctypes.byref(rs))
+            if a == 0:
+                self.samples.append((t, float(clk.value), pw.value / 1000.0 if b == 0 else None,
+                                     rs.value if c == 0 else 0))
+            time.sleep(period)
+
+    def stop(self):
+        self._stop.set()
+
+    def summary(self, t0, t1):
+        rows = [s for s in self.samples if t0 <= s[0] <= t1]
+        window = "timed region"
+        if not rows:
+            rows, window = list(self.samples), "whole run"
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["unsampled"],
+                    "samples": 0}
+        sm = sorted(r[1] for r in rows)
+        bits = 0
+        for r in rows:
+            bits |= r[3]
+        reasons = sorted(n for b, n in self.REASONS.items() if bits & b)
+        pw = [r[2] for r in rows if r[2] is not None]
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": self.max_mhz, "reasons": reasons,
+                "power_w_max": max(pw) if pw else None, "samples": len(rows), "window": window}
+
+
+# ----------------------------------------------------------------- helpers
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def _cpu_baseline(seconds_target=10.0):
+    """Oracle (plain single-threaded C) on a bounded sample of the workload:
+    whole rows of each family, with the per-tensor amax of the sampled rows."""
+    import torch
+
+    import oracle
+    import workloads
+    ocfg = oracle.Config(four_over_six=True, mse=True, err_f16=False, bound=448,
+                         amax_is_input=False)
+    rows = 64
+    done_rows, t_total = 0, 0.0
+    fam_i = 0
+    while t_total < seconds_target and done_rows < 4 * ROWS:
+        fam = workloads.FAMILIES[fam_i % 4]
+        x = workloads.activation(rows, COLS, fam, seed=fam_i, dtype=torch.bfloat16)
+        xf = x.float().numpy()
+        t = time.perf_counter()
+        oracle.quantize(xf, ocfg)
+        t_total += time.perf_counter() - t
+        done_rows += rows
+        fam_i += 1
+        rows = min(2048, rows * 2)
+    elems = done_rows * COLS
+    gbs = elems * BYTES_PER_ELEM / t_total / 1e9
+    return {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "elements_per_s": round(elems / t_total, 1),
+            "sample": "%d rows x %d cols of the four bf16 families (amax + 4over6 MSE encode), "
+                      "%.1f s of single-thread CPU time" % (done_rows, COLS, t_total)}
+
+
+def _time_events(fn, reps, stream):
+    import torch
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(reps):
+        fn()
+    e1.record(stream)
+    e1.synchronize()
+    return e0.elapsed_time(e1) / reps
+
+
+# ----------------------------------------------------------------- our arm
+def run_fos(args):
+    import torch
+    import torch.distributed as dist
+
+    import __graft_entry__
+    import workloads
+    __graft_entry__.build()
+    import nvfp4_quantization_precision_gb300 as fos
+
+    ws, rank, local = _dist()
+    torch.cuda.set_device(local)
+    if ws > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+    peak, peak_kind = _peaks()
+
+    xs = [workloads.activation(ROWS, COLS, f, seed=rank * 17 + i, dtype=torch.bfloat16, device=dev)
+          for i, f in enumerate(workloads.FAMILIES)]
+    amax = [torch.zeros(1, dtype=torch.float32, device=dev) for _ in xs]
+    codes = [torch.empty(ROWS, COLS // 2, dtype=torch.uint8, device=dev) for _ in xs]
+    scales = [torch.empty(ROWS, COLS // 16, dtype=torch.uint8, device=dev) for _ in xs]
+    cfg = fos.Config(four_over_six=True, mse=True, err_f16=False, bound=448)
+    L = fos.lib()
+    import ctypes
+    cc = cfg.c(True)
+    sp = ctypes.c_void_p(stream.cuda_stream)
+    xp = [ctypes.c_void_p(x.data_ptr()) for x in xs]
+    ap = [ctypes.c_void_p(a.data_ptr()) for a in amax]
+    cp = [ctypes.c_void_p(c.data_ptr()) for c in codes]
+    spp = [ctypes.c_void_p(s.data_ptr()) for s in scales]
+    ev_enc = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+
+    def amax_phase():
+        for i in range(4):
+            rc = L.fos_amax(xp[i], fos.FOS_BF16, ROWS, COLS, 0, ap[i], sp)
+            assert rc == 0, rc
+
+    def encode_phase():
+        for i in range(4):
+            rc = L.fos_quantize(xp[i], fos.FOS_BF16, ROWS, COLS, ctypes.byref(cc), ap[i], cp[i],
+                                spp[i], sp)
+            assert rc == 0, rc
+
+    def step(k=None):
+        amax_phase()
+        if k is not None:
+            ev_enc[k][0].record(stream)
+        encode_phase()
+        if k is not None:
+            ev_enc[k][1].record(stream)
+
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+        uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+    except Exception:
+        uuid = None
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    index = int(vis.split(",")[local]) if vis and vis.split(",")[local].isdigit() else local
+    clocks = ClockSampler(uuid, index)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for k in range(args.steps):
+        step(k)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    if ws > 1:
+        dist.barrier()
+    ms = e0.elapsed_time(e1) / args.steps
+    enc_ms = sum(a.elapsed_time(b) for a, b in ev_enc) / (4 * args.steps)
+    clock_summary = clocks.summary(t_wall0, t_wall1)
+    if ws > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+
+    units = ws * 4  # tensors processed per step, all ranks
+    value = units * ALG_BYTES / (ms / 1e3) / 1e9
+    out = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded families F1-F4, generated on device)",
+        "config": {"workload": WORKLOAD, "tensors_per_step_per_gpu": 4,
+                   "l2": "inputs larger than L2: 4 x 64 MiB per step, 2x the 129 MB L2",
+                   "bytes_per_tensor": ALG_BYTES},
+        "pct_of_peak": round(100.0 * value / ws / peak, 2),
+        "elements_per_s": round(units * ELEMS / (ms / 1e3), 1),
+        "gpu_launches": 8 * args.steps,
+    }
+    achieved = ALG_BYTES / (enc_ms / 1e3) / 1e9
+    out["roofline"] = {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
+                       "unit": "GB/s", "frac": round(achieved / peak, 4),
+                       "traffic": _profiled_traffic(), "kernel": "k_quant1x16<bf16,MSE,TENSOR>",
+                       "launch_ms": round(enc_ms, 5), "peak_kind": peak_kind + " (burst copy)"}
+    out["clocks"] = clock_summary
+
+    if rank == 0 and ws == 1 and not args.skip_extras:
+        out["e2e"] = _e2e(fos, L, xs, cfg, stream, args)
+        out["rows"] = _rows(fos, L, xs, stream, peak)
+        out["cpu_baseline"] = _cpu_baseline(args.cpu_seconds)
+    clocks.stop()
+    if ws > 1:
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(out))
+
+
+def _e2e(fos, L, xs, cfg, stream, args):
+    """Same step through the C ABI from pinned host buffers: H2D of the four
+    inputs, amax + encode, D2H of codes and scales, all inside the region."""
+    import ctypes
+
+    import torch
+    dev = xs[0].device
+    hx = [x.cpu().pin_memory() for x in xs]
+    dx = [torch.empty_like(x) for x in xs]
+    am = [torch.zeros(1, dtype=torch.float32, device=dev) for _ in xs]
+    dc = [torch.empty(ROWS, COLS // 2, dtype=torch.uint8, device=dev) for _ in xs]
+    ds = [torch.empty(ROWS, COLS // 16, dtype=torch.uint8, device=dev) for _ in xs]
+    hc = [torch.empty(ROWS, COLS // 2, dtype=torch.uint8).pin_memory() for _ in xs]
+    hs = [torch.empty(ROWS, COLS // 16, dtype=torch.uint8).pin_memory() for _ in xs]
+    cc = cfg.c(False)
+    sp = ctypes.c_void_p(stream.cuda_stream)
+
+    def step():
+        for i in range(4):
+            dx[i].copy_(hx[i], non_blocking=True)
+            rc = L.fos_quantize(ctypes.c_void_p(dx[i].data_ptr()), fos.FOS_BF16, ROWS, COLS,
+                                ctypes.byref(cc), ctypes.c_void_p(am[i].data_ptr()),
+                                ctypes.c_void_p(dc[i].data_ptr()),
+                                ctypes.c_void_p(ds[i].data_ptr()), sp)
+            assert rc == 0
+            hc[i].copy_(dc[i], non_blocking=True)
+            hs[i].copy_(ds[i], non_blocking=True)
+
+    reps = max(3, args.steps // 10)
+    for _ in range(3):
+        step()
+    ms = _time_events(step, reps, stream)
+    h2d = 4 * ELEMS * 2
+    d2h = 4 * (ELEMS // 2 + ELEMS // 16)
+    return {"value": round(4 * ALG_BYTES / (ms / 1e3) / 1e9, 2), "unit": "GB/s",
+            "ms_per_step": round(ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "steps": reps}
+
+
+def _rows(fos, L, xs, stream, peak):
+    """Kernel-only throughput of every hot-path row at its workload size
+    (inputs rotated over the four tensors, or larger than L2)."""
+    import torch
+
+    import workloads
+    dev = xs[0].device
+    res = {}
+    reps = 20
+    am = [fos.amax(x) for x in xs]
+    torch.cuda.synchronize()
+    # a1: amax pass
+    ms = _time_events(lambda it=iter(range(10 ** 9)): fos.amax(xs[next(it) % 4], out=am[0]),
+                      reps, stream)
+    res["amax_pass"] = {"GB/s": round(ELEMS * 2 / (ms / 1e3) / 1e9, 1), "ms": round(ms, 5)}
+    # a3-a8: encode sweep, amax given
+    sweep = {}
+    codes = torch.empty(ROWS, COLS // 2, dtype=torch.uint8, device=dev)
+    scales = torch.empty(ROWS, COLS // 16, dtype=torch.uint8, device=dev)
+    ra = [fos.amax(x, row_scaled=True) for x in xs]
+    for four, mse, f16, bound, row in (
+            [(False, True, False, 448, False), (False, True, False, 448, True)] +
+            [(True, m, h, b, r) for m in (False, True) for h in (False, True)
+             for b in (448, 256) for r in (False, True)]):
+        c = fos.Config(four_over_six=four, mse=mse, err_f16=f16, bound=bound, row_scaled=row)
+        it = iter(range(10 ** 9))
+        a = ra if row else am
+
+        def f():
+            i = next(it) % 4
+            fos.quantize(xs[i], c, amax=a[i], codes=codes, scales=scales)
+        f()
+        ms = _time_events(f, reps, stream)
+        name = ("std" if not four else ("mse" if mse else "mae") + ("_f16" if f16 else "_exact")
+                ) + "_%d_%s" % (bound, "row" if row else "tensor")
+        sweep[name] = round(ALG_BYTES / (ms / 1e3) / 1e9, 1)
+    res["encode_sweep_GB/s"] = sweep
+    # a9: fused QDQ at the metric shape and on the 8 x 2048x7168 weight list
+    for label, tensors in (("qdq_8192x4096_bf16", xs),
+                           ("qdq_list_8x2048x7168_bf16",
+                            workloads.qdq_weights(8, 2048, 7168, seed=0, device=dev))):
+        amx = [fos.amax(t) for t in tensors]
+        outs = [torch.empty_like(t) for t in tensors]
+        for mode in ("std", "mse_f16"):
+            c = fos.Config(four_over_six=(mode != "std"), mse=True, err_f16=(mode != "std"))
+            if label.startswith("qdq_list"):
+                def f():
+                    fos.qdq(tensors, c, amaxes=amx, outs=outs)
+                nbytes = sum(t.numel() for t in tensors) * 4
+            else:
+                it = iter(range(10 ** 9))
+
+                def f():
+                    i = next(it) % 4
+                    fos.qdq([tensors[i]], c, amaxes=[amx[i]], outs=[outs[i]])
+                nbytes = ELEMS * 4
+            f()
+            ms = _time_events(f, reps, stream)
+            res["%s_%s" % (label, mode)] = {"GB/s": round(nbytes / (ms / 1e3) / 1e9, 1),
+                                             "ms": round(ms, 5)}
+        del outs
+    # a11: dequantize back to bf16
+    c = fos.Config()
+    cs = [fos.quantize(x, c, amax=a) for x, a in zip(xs, am)]
+    out = torch.empty(ROWS, COLS, dtype=torch.bfloat16, device=dev)
+    it = iter(range(10 ** 9))
+
+    def f():
+        i = next(it) % 4
+        fos.dequantize(cs[i][0], cs[i][1], am[i], c, out=out)
+    f()
+    ms = _time_events(f, reps, stream)
+    res["dequantize_bf16"] = {"GB/s": round(ALG_BYTES / (ms / 1e3) / 1e9, 1), "ms": round(ms, 5)}
+    del cs
+    # a10: grouped MoE activations, 65536 x 7168 in 64 groups, per-group amax
+    R, C = 65536, 7168
+    offs = workloads.moe_offsets(R, 64, seed=0).to(dev)
+    xa = workloads.moe_activations(R, C, offs.cpu(), seed=0, device=dev)
+    ga = torch.empty(64, dtype=torch.float32, device=dev)
+    gc = torch.empty(R, C // 2, dtype=torch.uint8, device=dev)
+    gs = torch.empty(R, C // 16, dtype=torch.uint8, device=dev)
+    c = fos.Config()
+    fos.quantize_grouped(xa, offs, c, codes=gc, scales=gs)
+    ms = _time_events(lambda: fos.quantize_grouped(xa, offs, c, group_amax=ga, codes=gc,
+                                                   scales=gs), 5, stream)
+    live = int(offs[-1].item())
+    gbytes = live * C * BYTES_PER_ELEM + (R - live) * C * (0.5 + 1 / 16)
+    res["grouped_moe_65536x7168_amax_given"] = {"GB/s": round(gbytes / (ms / 1e3) / 1e9, 1),
+                                                "ms": round(ms, 4)}
+    del xa, gc, gs
+    # 16x16 weight quantize 14336 x 4096 bf16
+    w = workloads.weight(14336, 4096, seed=0, device=dev)
+    wa = fos.amax(w)
+    c = fos.Config(block16x16=True)
+    wc = torch.empty(14336, 2048, dtype=torch.uint8, device=dev)
+    ws_ = torch.empty(896, 256, dtype=torch.uint8, device=dev)
+    fos.quantize(w, c, amax=wa, codes=wc, scales=ws_)
+    ms = _time_events(lambda: fos.quantize(w, c, amax=wa, codes=wc, scales=ws_), reps, stream)
+    wbytes = 14336 * 4096 * (2 + 0.5 + 1 / 256)
+    res["weight_16x16_14336x4096_bf16"] = {"GB/s": round(wbytes / (ms / 1e3) / 1e9, 1),
+                                           "ms": round(ms, 5)}
+    for v in res.values():
+        if isinstance(v, dict) and "GB/s" in v:
+            v["frac"] = round(v["GB/s"] / peak, 3)
+    return res
+
+
+# ----------------------------------------------------------------- reference arm
+def run_reference(args):
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return
+    import torch
+
+    import oracle
+    import workloads
+    oracle.lib()
+    ocfg = oracle.Config(four_over_six=True, mse=True, err_f16=False, bound=448)
+    rows = 32  # per family and step: a bounded sample of the 8192 rows
+    batch = [workloads.activation(rows, COLS, f, seed=i, dtype=torch.bfloat16).float().numpy()
+             for i, f in enumerate(workloads.FAMILIES)]
+
+    def step():
+        for x in batch:
+            oracle.quantize(x, ocfg)
+    for _ in range(args.warmup):
+        step()
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    sec = (time.perf_counter() - t) / args.steps
+    elems = 4 * rows * COLS
+    val = elems * BYTES_PER_ELEM / sec / 1e9
+    sample = ("%d of 8192 rows x %d cols of each of the four bf16 families per step "
+              "(amax + 4over6 MSE encode), single-thread C oracle" % (rows, COLS))
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(val, 5), "unit": "GB/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(sec * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "sample_rows_per_tensor": rows},
+        "elements_per_s": round(elems / sec, 1),
+        "cpu_baseline": {"value": round(val, 5), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(val, 5), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0}}))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="fos", choices=["fos", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--skip-extras", action="store_true",
+                    help="only the timed step (no e2e / per-row / CPU baseline)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_fos(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,180 @@
+/*
+ * fos.h -- C ABI of the GB300 (sm_103a) NVFP4 four-over-six block quantizer.
+ *
+ * The method (torchao PR "Add the four-over-six grouped GEMM and dispatcher
+ * wiring", description and first commit): every quantization block -- 1x16
+ * elements along a row, or a 16x16 tile for weights -- is encoded twice under
+ * an FP32 global scale, once as standard NVFP4 (block amax mapped to E2M1
+ * value 6 by an E4M3 block scale) and once as a 1.5x-scale candidate (block
+ * amax mapped to 4).  Both are rounded to E2M1 with correctly-rounded FP32
+ * division, decoded exactly, and compared by MAE or MSE; the lower-error
+ * candidate's packed E2M1 codes and E4M3 scale are stored (torchao PR "Add a
+ * CuTe DSL fast-path kernel for four-over-six quantize": pinned rounding,
+ * pinned width-16 error reduction, NaN-dropping block amax, NaN -> +6).
+ *
+ * Conventions shared by every entry point
+ *   - Data pointers (x, out, codes, scales, amax, offs) are DEVICE pointers
+ *     owned by the caller; the library never allocates, frees or keeps them.
+ *     Host-side arrays (the pointer / size lists of fos_qdq) are read during
+ *     the call only.
+ *   - Tensors are row-major and contiguous: x is [rows, cols]; codes are
+ *     [rows, cols/2] bytes, element 2j in the low nibble of byte j; scales are
+ *     E4M3 bytes [rows, cols/16] (1x16) or [rows/16, cols/16] (16x16), plain
+ *     row-major (no GEMM swizzle).
+ *   - cols % 16 == 0; with 16x16 blocks also rows % 16 == 0.
+ *   - x / out must be 32-byte aligned, codes 8-byte aligned (any row slice of
+ *     a tensor from the CUDA caching allocator satisfies this).
+ *   - Work is enqueued on `stream` of the device that owns the data and the
+ *     call returns without synchronising the host.  The caller's current
+ *     device is restored before return.
+ *   - Every argument is validated on the host before anything is launched;
+ *     a failed check returns an error status and launches nothing.  CUDA
+ *     launch failures return FOS_ERR_CUDA.  Kernels never trap and never
+ *     wait on other work, so no call can hang the device.
+ *   - Global scale (reading of "FP32 global scale"): S = (6 * bound) / A,
+ *     correctly rounded, for a global amax A; S = 1 when A is zero, negative,
+ *     NaN or Inf; S = FLT_MAX when the quotient overflows.
+ */
+#ifndef FOS_H
+#define FOS_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define FOS_API __attribute__((visibility("default")))
+#else
+#define FOS_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Identical to cudaStream_t; 0 is the legacy default stream. */
+typedef struct CUstream_st* fos_stream_t;
+
+typedef enum {
+    FOS_OK = 0,
+    FOS_ERR_INVALID_ARG = 1, /* null pointer, negative size, bad enum value   */
+    FOS_ERR_UNSUPPORTED = 2, /* shape / knob / dtype combination not offered  */
+    FOS_ERR_MISALIGNED = 3,  /* pointer alignment rule above violated         */
+    FOS_ERR_CUDA = 4         /* a CUDA runtime call or launch failed          */
+} fos_status;
+
+typedef enum { FOS_BF16 = 0, FOS_FP16 = 1, FOS_FP32 = 2 } fos_dtype;
+
+enum { FOS_BLOCK_1X16 = 0, FOS_BLOCK_16X16 = 1 };
+enum { FOS_MODE_STANDARD = 0, FOS_MODE_4OVER6 = 1 };
+enum { FOS_MAE = 0, FOS_MSE = 1 };
+enum { FOS_ERR_EXACT_F32 = 0, FOS_ERR_F16 = 1 };
+enum { FOS_SCALE_TENSOR = 0, FOS_SCALE_ROW = 1 };
+
+/* The knobs the pages name (Megatron PR "Fuse NVFP4 fake-QAT quantize-
+ * dequantize with CuTe DSL", numerical contract: standard NVFP4 plus 4over6
+ * MAE/MSE, E4M3 256/448, exact-error / FP16-error; torchao PRs: 1x16 / 16x16
+ * blocks, per-tensor or row-scaled global scale). */
+typedef struct {
+    int block;         /* FOS_BLOCK_1X16 | FOS_BLOCK_16X16                       */
+    int mode;          /* FOS_MODE_STANDARD (map-to-6 only) | FOS_MODE_4OVER6    */
+    int err_metric;    /* FOS_MAE | FOS_MSE                     (4over6 only)    */
+    int err_precision; /* FOS_ERR_EXACT_F32 | FOS_ERR_F16       (4over6 only)    */
+    int e4m3_bound;    /* 448 | 256: E4M3 value the global scale maps the amax to */
+    int granularity;   /* FOS_SCALE_TENSOR | FOS_SCALE_ROW                       */
+    int amax_is_input; /* 1: caller supplies amax; 0: library computes, writes it */
+} fos_config;
+
+/*
+ * fos_amax -- global amax pass (Megatron PR, fused data path: FP32
+ * per-tensor amax computed before the fused kernel).  NaN-dropping max|x|
+ * with initial +0: a NaN never becomes the amax and an all-NaN or empty
+ * scope gives 0.
+ *   granularity FOS_SCALE_TENSOR: amax[0] = over all of x.
+ *   granularity FOS_SCALE_ROW:    amax[r] = over row r, r < rows.
+ * Errors: FOS_ERR_INVALID_ARG (null pointers with nonzero size, negative
+ * sizes, bad enum), FOS_ERR_UNSUPPORTED (cols % 16 != 0), FOS_ERR_MISALIGNED.
+ */
+FOS_API fos_status fos_amax(const void* x, fos_dtype dt, int64_t rows, int64_t cols, int granularity,
+                    float* amax, fos_stream_t stream);
+
+/*
+ * fos_quantize -- four-over-six (or standard) NVFP4 quantize of x [rows, cols]
+ * of dtype bf16, fp16 or fp32 (torchao fast-path PR: the quantizer op;
+ * grouped PR: per-tensor or row-scaled global scale, 1x16 / 16x16 blocks).
+ *   amax   [1] (FOS_SCALE_TENSOR) or [rows] (FOS_SCALE_ROW): read when
+ *          cfg->amax_is_input, otherwise computed first and written.
+ *          With 16x16 blocks and FOS_SCALE_ROW the per-row amax must be
+ *          uniform inside each 16-row tile (grouped PR, tile-uniform
+ *          contract); each tile uses the amax of its first row.
+ *   codes  [rows, cols/2] out; scales out (layout above).
+ * Errors as for fos_amax, plus FOS_ERR_UNSUPPORTED for a bad bound, block,
+ * mode or (16x16) rows % 16 != 0.
+ */
+FOS_API fos_status fos_quantize(const void* x, fos_dtype dt, int64_t rows, int64_t cols,
+                        const fos_config* cfg, float* amax, uint8_t* codes, uint8_t* scales,
+                        fos_stream_t stream);
+
+/*
+ * fos_dequantize -- standard NVFP4 decode (grouped PR, first commit:
+ * "nvfp4_dequantize: the standard NVFP4 decode (recipe-agnostic)"):
+ *   out = round_to(out_dt, e2m1(code) * (e4m3(scale) / S)),
+ * with S recomputed from amax and cfg->e4m3_bound exactly as fos_quantize
+ * does; the candidate choice need not be stored.  cfg->block and
+ * cfg->granularity select the scale layout and the amax indexing;
+ * mode / metric / precision are ignored.  out is [rows, cols] of out_dt.
+ */
+FOS_API fos_status fos_dequantize(const uint8_t* codes, const uint8_t* scales, const float* amax,
+                          int64_t rows, int64_t cols, const fos_config* cfg, void* out,
+                          fos_dtype out_dt, fos_stream_t stream);
+
+/*
+ * fos_qdq -- fused fake-QAT quantize-dequantize of a list of n discrete
+ * rank-2 tensors (Megatron PR: "General list API" and "Fused data path":
+ * codes and E4M3 scales stay in registers; only the dequantized BF16/FP16
+ * result is written).  The whole list is processed in one kernel launch
+ * (lists longer than FOS_QDQ_MAX_LIST are split into several launches).
+ *   x[i], out[i]: device pointers, rows[i] x cols[i], dtype dt (bf16 or
+ *   fp16; out has the same dtype).  amax[i]: device pointer to one float,
+ *   the per-tensor amax: read when cfg->amax_is_input, else computed and
+ *   written first.  Only 1x16 blocks and FOS_SCALE_TENSOR (the pages'
+ *   non-goals exclude 2D blocks and row scaling for this path).
+ * The host arrays x, out, rows, cols, amax must hold n entries each.
+ * Result equals fos_dequantize(fos_quantize(x)) bit for bit.
+ */
+#define FOS_QDQ_MAX_LIST 64
+FOS_API fos_status fos_qdq(int n, const void* const* x, void* const* out, const int64_t* rows,
+                   const int64_t* cols, float* const* amax, fos_dtype dt,
+                   const fos_config* cfg, fos_stream_t stream);
+
+/*
+ * fos_quantize_grouped -- one call over a packed MoE token tensor (grouped
+ * PR, third commit: "each token group's amax expands to a per-row vector so
+ * the whole packed tensor quantizes in one call, bitwise identical to
+ * quantizing each group separately"; expert weights flatten to one call).
+ *   offs: device int32 [G], cumulative group ends.  Group g covers rows
+ *   [end_{g-1}, end_g) with end_{-1} = 0 and end_g = clamp(offs[g],
+ *   end_{g-1}, rows).  Rows at or past end_{G-1} (the over-allocated tail of
+ *   a padded token dispatcher) are not read; their codes and scales are 0.
+ *   With 16x16 blocks offs entries should be multiples of 16; a tile belongs
+ *   to the group of its first row.
+ *   group_amax: device float [G]; read when cfg->amax_is_input, otherwise
+ *   computed (NaN-dropping, empty group -> 0) and written.
+ *   cfg->granularity is ignored (the group amax is the global scale source).
+ *   1 <= G <= FOS_GROUPED_MAX_GROUPS.
+ */
+#define FOS_GROUPED_MAX_GROUPS 8192
+FOS_API fos_status fos_quantize_grouped(const void* x, fos_dtype dt, int64_t rows, int64_t cols,
+                                const int32_t* offs, int G, const fos_config* cfg,
+                                float* group_amax, uint8_t* codes, uint8_t* scales,
+                                fos_stream_t stream);
+
+/* Static, human-readable name of a status code. */
+FOS_API const char* fos_status_string(fos_status s);
+
+/* Library version as major * 10000 + minor * 100 + patch. */
+FOS_API int fos_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FOS_H */

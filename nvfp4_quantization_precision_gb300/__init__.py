@@ -1,0 +1,223 @@
+"""NVFP4 four-over-six block quantizer for GB300 -- Python binding.
+
+Argument marshalling only: every step of the quantizer runs in the CUDA
+kernels of ``libfos.so`` (C ABI in ``include/fos.h``).  PyTorch supplies the
+device memory and the current stream.  There is no CPU path: if the library
+is not built, or a tensor is not on a CUDA device, the call raises.
+
+Entry points (names follow the C ABI):
+  amax(x, granularity)                      -> float32 amax
+  quantize(x, ...)                          -> (codes, scales, amax)
+  dequantize(codes, scales, amax, ...)      -> tensor
+  qdq(xs, ...)                              -> list of tensors (one launch)
+  quantize_grouped(x, offs, ...)            -> (codes, scales, group_amax)
+"""
+import ctypes
+import os
+from dataclasses import dataclass
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libfos.so")
+
+FOS_OK, FOS_ERR_INVALID_ARG, FOS_ERR_UNSUPPORTED, FOS_ERR_MISALIGNED, FOS_ERR_CUDA = range(5)
+FOS_BF16, FOS_FP16, FOS_FP32 = 0, 1, 2
+QDQ_MAX_LIST = 64
+GROUPED_MAX_GROUPS = 8192
+
+_DT = {torch.bfloat16: FOS_BF16, torch.float16: FOS_FP16, torch.float32: FOS_FP32}
+_NAMES = ("fos_amax", "fos_quantize", "fos_dequantize", "fos_qdq", "fos_quantize_grouped",
+          "fos_status_string", "fos_version", "fos_diag_convert")
+
+
+class FosError(RuntimeError):
+    def __init__(self, status, what):
+        self.status = status
+        super().__init__("%s failed: %s (status %d)" % (what, status_string(status), status))
+
+
+class FosConfig(ctypes.Structure):
+    _fields_ = [("block", ctypes.c_int), ("mode", ctypes.c_int), ("err_metric", ctypes.c_int),
+                ("err_precision", ctypes.c_int), ("e4m3_bound", ctypes.c_int),
+                ("granularity", ctypes.c_int), ("amax_is_input", ctypes.c_int)]
+
+
+@dataclass(frozen=True)
+class Config:
+    """Knobs of the quantizer (see include/fos.h)."""
+    block16x16: bool = False
+    four_over_six: bool = True
+    mse: bool = True
+    err_f16: bool = False
+    bound: int = 448
+    row_scaled: bool = False
+
+    def c(self, amax_is_input):
+        return FosConfig(int(self.block16x16), int(self.four_over_six), int(self.mse),
+                         int(self.err_f16), int(self.bound), int(self.row_scaled),
+                         int(bool(amax_is_input)))
+
+
+_lib = None
+
+
+def lib():
+    """The loaded libfos.so; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError("libfos.so is not built (run __graft_entry__.build() or "
+                               "python -m nvfp4_quantization_precision_gb300.build)")
+        L = ctypes.CDLL(LIB_PATH)
+        P, I64, I = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+        CFG = ctypes.POINTER(FosConfig)
+        L.fos_amax.argtypes = [P, I, I64, I64, I, P, P]
+        L.fos_quantize.argtypes = [P, I, I64, I64, CFG, P, P, P, P]
+        L.fos_dequantize.argtypes = [P, P, P, I64, I64, CFG, P, I, P]
+        L.fos_qdq.argtypes = [I, P, P, P, P, P, I, CFG, P]
+        L.fos_quantize_grouped.argtypes = [P, I, I64, I64, P, I, CFG, P, P, P, P]
+        L.fos_diag_convert.argtypes = [I, P, P, I64, P]
+        for n in ("fos_amax", "fos_quantize", "fos_dequantize", "fos_qdq",
+                  "fos_quantize_grouped", "fos_diag_convert"):
+            getattr(L, n).restype = ctypes.c_int
+        L.fos_status_string.argtypes = [I]
+        L.fos_status_string.restype = ctypes.c_char_p
+        L.fos_version.restype = ctypes.c_int
+        _lib = L
+    return _lib
+
+
+def status_string(s):
+    return lib().fos_status_string(int(s)).decode()
+
+
+def _check(rc, what):
+    if rc != FOS_OK:
+        raise FosError(rc, what)
+
+
+def _stream(t):
+    return ctypes.c_void_p(torch.cuda.current_stream(t.device).cuda_stream)
+
+
+def _cuda(t, name):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+
+
+def _p(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+
+
+def amax(x, row_scaled=False, out=None):
+    """NaN-dropping max|x| per tensor ([1]) or per row ([rows]), float32."""
+    _cuda(x, "x")
+    R, C = x.shape
+    n = R if row_scaled else 1
+    if out is None:
+        out = torch.empty(n, dtype=torch.float32, device=x.device)
+    _check(lib().fos_amax(_p(x), _DT[x.dtype], R, C, int(row_scaled), _p(out), _stream(x)),
+           "fos_amax")
+    return out
+
+
+def scales_shape(rows, cols, block16x16):
+    return (rows // 16 if block16x16 else rows, cols // 16)
+
+
+def quantize(x, cfg=Config(), amax=None, codes=None, scales=None):
+    """Quantize x [rows, cols] (bf16 / fp16 / fp32).  With amax=None the
+    library computes the amax (per tensor or per row) and returns it."""
+    _cuda(x, "x")
+    R, C = x.shape
+    dev = x.device
+    given = amax is not None
+    if amax is None:
+        amax = torch.empty(R if cfg.row_scaled else 1, dtype=torch.float32, device=dev)
+    if codes is None:
+        codes = torch.empty((R, C // 2), dtype=torch.uint8, device=dev)
+    if scales is None:
+        scales = torch.empty(scales_shape(R, C, cfg.block16x16), dtype=torch.uint8, device=dev)
+    cc = cfg.c(given)
+    _check(lib().fos_quantize(_p(x), _DT[x.dtype], R, C, ctypes.byref(cc), _p(amax), _p(codes),
+                              _p(scales), _stream(x)), "fos_quantize")
+    return codes, scales, amax
+
+
+def dequantize(codes, scales, amax, cfg=Config(), out_dtype=torch.bfloat16, out=None):
+    _cuda(codes, "codes")
+    R, C2 = codes.shape
+    C = 2 * C2
+    if out is None:
+        out = torch.empty((R, C), dtype=out_dtype, device=codes.device)
+    cc = cfg.c(True)
+    _check(lib().fos_dequantize(_p(codes), _p(scales), _p(amax), R, C, ctypes.byref(cc), _p(out),
+                                _DT[out.dtype], _stream(codes)), "fos_dequantize")
+    return out
+
+
+def qdq(xs, cfg=Config(), amaxes=None, outs=None):
+    """Fused quantize-dequantize of a list of rank-2 bf16/fp16 tensors in one
+    launch.  amaxes: list of 1-element float32 tensors (given) or None (the
+    library computes them).  Returns the list of outputs."""
+    n = len(xs)
+    if n == 0:
+        return []
+    for x in xs:
+        _cuda(x, "x")
+    dt = xs[0].dtype
+    given = amaxes is not None
+    if amaxes is None:
+        amaxes = [torch.empty(1, dtype=torch.float32, device=x.device) for x in xs]
+    if outs is None:
+        outs = [torch.empty_like(x) for x in xs]
+    P = ctypes.c_void_p * n
+    xp = P(*[x.data_ptr() for x in xs])
+    op = P(*[o.data_ptr() for o in outs])
+    ap = P(*[a.data_ptr() for a in amaxes])
+    rows = (ctypes.c_int64 * n)(*[x.shape[0] for x in xs])
+    cols = (ctypes.c_int64 * n)(*[x.shape[1] for x in xs])
+    cc = cfg.c(given)
+    _check(lib().fos_qdq(n, xp, op, rows, cols, ap, _DT[dt], ctypes.byref(cc), _stream(xs[0])),
+           "fos_qdq")
+    return outs
+
+
+def quantize_grouped(x, offs, cfg=Config(), group_amax=None, codes=None, scales=None):
+    """One call over a packed token tensor split into groups by cumulative
+    ends offs (int32, device).  Rows past offs[-1] get zero codes/scales."""
+    _cuda(x, "x")
+    _cuda(offs, "offs")
+    if offs.dtype != torch.int32:
+        raise ValueError("offs must be int32")
+    R, C = x.shape
+    G = offs.numel()
+    dev = x.device
+    given = group_amax is not None
+    if group_amax is None:
+        group_amax = torch.empty(G, dtype=torch.float32, device=dev)
+    if codes is None:
+        codes = torch.empty((R, C // 2), dtype=torch.uint8, device=dev)
+    if scales is None:
+        scales = torch.empty(scales_shape(R, C, cfg.block16x16), dtype=torch.uint8, device=dev)
+    cc = cfg.c(given)
+    _check(lib().fos_quantize_grouped(_p(x), _DT[x.dtype], R, C, _p(offs), G, ctypes.byref(cc),
+                                      _p(group_amax), _p(codes), _p(scales), _stream(x)),
+           "fos_quantize_grouped")
+    return codes, scales, group_amax
+
+
+DIAG_E2M1_ENCODE, DIAG_E2M1_DECODE, DIAG_E4M3_ENCODE, DIAG_E4M3_DECODE = 0, 1, 2, 3
+DIAG_F16_ROUND, DIAG_BF16_BITS, DIAG_F16_BITS, DIAG_DIV6 = 4, 5, 6, 7
+
+
+def diag_convert(op, inp, out):
+    """Element-wise access to one device conversion primitive (fos_diag.h)."""
+    _cuda(inp, "inp")
+    _cuda(out, "out")
+    _check(lib().fos_diag_convert(int(op), _p(inp), _p(out), inp.numel(), _stream(inp)),
+           "fos_diag_convert")
+    return out

@@ -1,0 +1,372 @@
+// fos_api.cu -- host side of the C ABI declared in include/fos.h.
+//
+// Every entry point validates all arguments before touching the CUDA
+// runtime, switches to the device that owns the data, enqueues its kernels on
+// the caller's stream and restores the caller's current device (the
+// Megatron fused-QDQ PR tests that the kernel "uses and restores" a
+// non-current device).  Nothing here allocates device memory or synchronises
+// the host.
+#include <cstdint>
+#include <cstring>
+
+#include "../../include/fos.h"
+#include "../../include/fos_diag.h"
+#include "fos_launch.cuh"
+
+using namespace fos;
+
+namespace {
+
+constexpr int kVersion = 10000;  // 1.0.0
+
+bool valid_dtype(int dt) { return dt == FOS_BF16 || dt == FOS_FP16 || dt == FOS_FP32; }
+
+fos_status check_config(const fos_config* cfg) {
+    if (!cfg) return FOS_ERR_INVALID_ARG;
+    if (cfg->block != FOS_BLOCK_1X16 && cfg->block != FOS_BLOCK_16X16) return FOS_ERR_INVALID_ARG;
+    if (cfg->mode != FOS_MODE_STANDARD && cfg->mode != FOS_MODE_4OVER6) return FOS_ERR_INVALID_ARG;
+    if (cfg->err_metric != FOS_MAE && cfg->err_metric != FOS_MSE) return FOS_ERR_INVALID_ARG;
+    if (cfg->err_precision != FOS_ERR_EXACT_F32 && cfg->err_precision != FOS_ERR_F16)
+        return FOS_ERR_INVALID_ARG;
+    if (cfg->granularity != FOS_SCALE_TENSOR && cfg->granularity != FOS_SCALE_ROW)
+        return FOS_ERR_INVALID_ARG;
+    if (cfg->amax_is_input != 0 && cfg->amax_is_input != 1) return FOS_ERR_INVALID_ARG;
+    if (cfg->e4m3_bound != 448 && cfg->e4m3_bound != 256) return FOS_ERR_UNSUPPORTED;
+    return FOS_OK;
+}
+
+Err err_of(const fos_config* cfg) {
+    if (cfg->mode == FOS_MODE_STANDARD) return Err::STD;
+    const bool mse = cfg->err_metric == FOS_MSE, h = cfg->err_precision == FOS_ERR_F16;
+    if (mse) return h ? Err::MSE_H : Err::MSE;
+    return h ? Err::MAE_H : Err::MAE;
+}
+
+fos_status check_shape(int64_t rows, int64_t cols, bool b16) {
+    if (rows < 0 || cols < 0) return FOS_ERR_INVALID_ARG;
+    if (cols % 16 != 0) return FOS_ERR_UNSUPPORTED;
+    if (b16 && rows % 16 != 0) return FOS_ERR_UNSUPPORTED;
+    // keeps every byte offset of the kernels inside int64
+    if (cols > 0 && rows > (int64_t)(INT64_C(1) << 40) / cols) return FOS_ERR_UNSUPPORTED;
+    return FOS_OK;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+// Device that owns a pointer, or -1 when the pointer is not device memory.
+int device_of(const void* p) {
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        cudaGetLastError();
+        return -1;
+    }
+    if (at.type != cudaMemoryTypeDevice && at.type != cudaMemoryTypeManaged) return -1;
+    return at.device;
+}
+
+// Switches to the device owning the data for the lifetime of the object.
+struct DeviceScope {
+    int prev = -1;
+    int dev = -1;
+    bool switched = false;
+    fos_status st = FOS_OK;
+    explicit DeviceScope(int d) : dev(d) {
+        if (cudaGetDevice(&prev) != cudaSuccess) {
+            cudaGetLastError();
+            st = FOS_ERR_CUDA;
+            return;
+        }
+        if (prev != dev) {
+            if (cudaSetDevice(dev) != cudaSuccess) {
+                cudaGetLastError();
+                st = FOS_ERR_CUDA;
+                return;
+            }
+            switched = true;
+        }
+    }
+    ~DeviceScope() {
+        if (switched) cudaSetDevice(prev);
+    }
+};
+
+// All listed device pointers must live on one device; returns it or -1.
+int common_device(std::initializer_list<const void*> ptrs) {
+    int dev = -1;
+    for (const void* p : ptrs) {
+        const int d = device_of(p);
+        if (d < 0) return -1;
+        if (dev >= 0 && d != dev) return -1;
+        dev = d;
+    }
+    return dev;
+}
+
+fos_status cuda_status(cudaError_t e) {
+    if (e == cudaSuccess) return FOS_OK;
+    cudaGetLastError();
+    return FOS_ERR_CUDA;
+}
+
+In in_of(fos_dtype dt) { return dt == FOS_BF16 ? In::BF16 : (dt == FOS_FP16 ? In::F16 : In::F32); }
+
+cudaError_t run_amax(const void* x, fos_dtype dt, int64_t rows, int64_t cols, Src scope,
+                     float* amax, const int32_t* offs, int G, cudaStream_t s) {
+    AmaxArgs a{};
+    a.x = x;
+    a.amax = amax;
+    a.offs = offs;
+    a.G = G;
+    a.rows = rows;
+    a.nb = cols / 16;
+    a.units = (rows * a.nb + 31) / 32;
+    if (scope == Src::TENSOR || scope == Src::GROUP) {
+        const size_t n = (scope == Src::TENSOR) ? 1 : (size_t)G;
+        cudaError_t e = cudaMemsetAsync(amax, 0, sizeof(float) * n, s);
+        if (e != cudaSuccess) return e;
+        if (rows == 0 || cols == 0) return cudaSuccess;
+    }
+    if (rows == 0) return cudaSuccess;
+    if (cols == 0) return cudaMemsetAsync(amax, 0, sizeof(float) * (size_t)rows, s);
+    return launch_amax(in_of(dt), scope, a, s);
+}
+
+cudaError_t run_quant(const void* x, fos_dtype dt, int64_t rows, int64_t cols,
+                      const fos_config* cfg, const float* amax, Src src, const int32_t* offs,
+                      int G, uint8_t* codes, uint8_t* scales, cudaStream_t s) {
+    if (rows == 0 || cols == 0) return cudaSuccess;
+    EncArgs a{};
+    a.x = x;
+    a.codes = codes;
+    a.scales = scales;
+    a.amax = amax;
+    a.offs = offs;
+    a.G = G;
+    a.rows = rows;
+    a.nb = cols / 16;
+    a.nblk = rows * a.nb;
+    a.six_bound = 6.0f * (float)cfg->e4m3_bound;
+    a.neg_zero = -0.0f;
+    const Err em = err_of(cfg);
+    const In it = in_of(dt);
+    if (cfg->block == FOS_BLOCK_16X16) {
+        a.cpr = (a.nb + 1) / 2;  // tile pairs per 16-row band
+        a.units = (rows / 16) * a.cpr;
+        switch (it) {
+            case In::BF16: return launch_quant16x16_bf16(em, src, a, s);
+            case In::F16: return launch_quant16x16_f16(em, src, a, s);
+            case In::F32: return launch_quant16x16_f32(em, src, a, s);
+        }
+    } else {
+        a.cpr = (a.nb + 31) / 32;
+        a.units = (src == Src::TENSOR) ? (a.nblk + 31) / 32 : rows * a.cpr;
+        switch (it) {
+            case In::BF16: return launch_quant1x16_bf16(em, src, a, s);
+            case In::F16: return launch_quant1x16_f16(em, src, a, s);
+            case In::F32: return launch_quant1x16_f32(em, src, a, s);
+        }
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* fos_status_string(fos_status s) {
+    switch (s) {
+        case FOS_OK: return "ok";
+        case FOS_ERR_INVALID_ARG: return "invalid argument";
+        case FOS_ERR_UNSUPPORTED: return "unsupported shape, knob or dtype";
+        case FOS_ERR_MISALIGNED: return "misaligned pointer";
+        case FOS_ERR_CUDA: return "CUDA runtime error";
+    }
+    return "unknown status";
+}
+
+int fos_version(void) { return kVersion; }
+
+fos_status fos_amax(const void* x, fos_dtype dt, int64_t rows, int64_t cols, int granularity,
+                    float* amax, fos_stream_t stream) {
+    if (!valid_dtype(dt)) return FOS_ERR_INVALID_ARG;
+    if (granularity != FOS_SCALE_TENSOR && granularity != FOS_SCALE_ROW) return FOS_ERR_INVALID_ARG;
+    fos_status st = check_shape(rows, cols, false);
+    if (st) return st;
+    if (!x || !amax) return FOS_ERR_INVALID_ARG;
+    if (!aligned(x, 32)) return FOS_ERR_MISALIGNED;
+    const int dev = common_device({x, amax});
+    if (dev < 0) return FOS_ERR_INVALID_ARG;
+    DeviceScope scope(dev);
+    if (scope.st) return scope.st;
+    const Src sc = granularity == FOS_SCALE_ROW ? Src::ROW : Src::TENSOR;
+    return cuda_status(run_amax(x, dt, rows, cols, sc, amax, nullptr, 0,
+                                reinterpret_cast<cudaStream_t>(stream)));
+}
+
+fos_status fos_quantize(const void* x, fos_dtype dt, int64_t rows, int64_t cols,
+                        const fos_config* cfg, float* amax, uint8_t* codes, uint8_t* scales,
+                        fos_stream_t stream) {
+    if (!valid_dtype(dt)) return FOS_ERR_INVALID_ARG;
+    fos_status st = check_config(cfg);
+    if (st) return st;
+    st = check_shape(rows, cols, cfg->block == FOS_BLOCK_16X16);
+    if (st) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const Src src = cfg->granularity == FOS_SCALE_ROW ? Src::ROW : Src::TENSOR;
+    if (rows == 0 || cols == 0) {  // nothing to encode; a computed amax is 0
+        if (cfg->amax_is_input || (src == Src::ROW && rows == 0)) return FOS_OK;
+        if (!amax) return FOS_ERR_INVALID_ARG;
+        const int d = device_of(amax);
+        if (d < 0) return FOS_ERR_INVALID_ARG;
+        DeviceScope scope(d);
+        if (scope.st) return scope.st;
+        const size_t n = (src == Src::ROW) ? (size_t)rows : 1;
+        return cuda_status(cudaMemsetAsync(amax, 0, sizeof(float) * n, s));
+    }
+    if (!x || !amax || !codes || !scales) return FOS_ERR_INVALID_ARG;
+    if (!aligned(x, 32) || !aligned(codes, 8)) return FOS_ERR_MISALIGNED;
+    const int dev = common_device({x, amax, codes, scales});
+    if (dev < 0) return FOS_ERR_INVALID_ARG;
+    DeviceScope scope(dev);
+    if (scope.st) return scope.st;
+    if (!cfg->amax_is_input) {
+        st = cuda_status(run_amax(x, dt, rows, cols, src, amax, nullptr, 0, s));
+        if (st) return st;
+    }
+    return cuda_status(run_quant(x, dt, rows, cols, cfg, amax, src, nullptr, 0, codes, scales, s));
+}
+
+fos_status fos_quantize_grouped(const void* x, fos_dtype dt, int64_t rows, int64_t cols,
+                                const int32_t* offs, int G, const fos_config* cfg,
+                                float* group_amax, uint8_t* codes, uint8_t* scales,
+                                fos_stream_t stream) {
+    if (!valid_dtype(dt)) return FOS_ERR_INVALID_ARG;
+    fos_status st = check_config(cfg);
+    if (st) return st;
+    st = check_shape(rows, cols, cfg->block == FOS_BLOCK_16X16);
+    if (st) return st;
+    if (G < 1) return FOS_ERR_INVALID_ARG;
+    if (G > FOS_GROUPED_MAX_GROUPS) return FOS_ERR_UNSUPPORTED;
+    if (!x || !offs || !group_amax || !codes || !scales) return FOS_ERR_INVALID_ARG;
+    if (!aligned(x, 32) || !aligned(codes, 8) || !aligned(offs, 4)) return FOS_ERR_MISALIGNED;
+    const int dev = common_device({x, offs, group_amax, codes, scales});
+    if (dev < 0) return FOS_ERR_INVALID_ARG;
+    DeviceScope scope(dev);
+    if (scope.st) return scope.st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (!cfg->amax_is_input) {
+        st = cuda_status(run_amax(x, dt, rows, cols, Src::GROUP, group_amax, offs, G, s));
+        if (st) return st;
+    }
+    return cuda_status(
+        run_quant(x, dt, rows, cols, cfg, group_amax, Src::GROUP, offs, G, codes, scales, s));
+}
+
+fos_status fos_dequantize(const uint8_t* codes, const uint8_t* scales, const float* amax,
+                          int64_t rows, int64_t cols, const fos_config* cfg, void* out,
+                          fos_dtype out_dt, fos_stream_t stream) {
+    if (!valid_dtype(out_dt)) return FOS_ERR_INVALID_ARG;
+    fos_status st = check_config(cfg);
+    if (st) return st;
+    const bool b16 = cfg->block == FOS_BLOCK_16X16;
+    st = check_shape(rows, cols, b16);
+    if (st) return st;
+    if (!codes || !scales || !amax || !out) return FOS_ERR_INVALID_ARG;
+    if (!aligned(out, 32) || !aligned(codes, 8)) return FOS_ERR_MISALIGNED;
+    const int dev = common_device({codes, scales, amax, out});
+    if (dev < 0) return FOS_ERR_INVALID_ARG;
+    DeviceScope scope(dev);
+    if (scope.st) return scope.st;
+    if (rows == 0 || cols == 0) return FOS_OK;
+    DeqArgs a{};
+    a.codes = codes;
+    a.scales = scales;
+    a.amax = amax;
+    a.out = out;
+    a.rows = rows;
+    a.nb = cols / 16;
+    a.cpr = (a.nb + 31) / 32;
+    a.units = rows * a.cpr;
+    a.six_bound = 6.0f * (float)cfg->e4m3_bound;
+    const Out ot = out_dt == FOS_BF16 ? Out::BF16 : (out_dt == FOS_FP16 ? Out::F16 : Out::F32);
+    const Src src = cfg->granularity == FOS_SCALE_ROW ? Src::ROW : Src::TENSOR;
+    return cuda_status(launch_dequant(ot, b16, src, a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+fos_status fos_qdq(int n, const void* const* x, void* const* out, const int64_t* rows,
+                   const int64_t* cols, float* const* amax, fos_dtype dt,
+                   const fos_config* cfg, fos_stream_t stream) {
+    if (n < 0) return FOS_ERR_INVALID_ARG;
+    if (dt != FOS_BF16 && dt != FOS_FP16) return valid_dtype(dt) ? FOS_ERR_UNSUPPORTED
+                                                                  : FOS_ERR_INVALID_ARG;
+    fos_status st = check_config(cfg);
+    if (st) return st;
+    if (cfg->block != FOS_BLOCK_1X16 || cfg->granularity != FOS_SCALE_TENSOR)
+        return FOS_ERR_UNSUPPORTED;
+    if (n == 0) return FOS_OK;
+    if (!x || !out || !rows || !cols || !amax) return FOS_ERR_INVALID_ARG;
+    for (int i = 0; i < n; ++i) {
+        st = check_shape(rows[i], cols[i], false);
+        if (st) return st;
+        const bool empty = rows[i] == 0 || cols[i] == 0;  // data pointers may be null
+        if (!amax[i] || (!empty && (!x[i] || !out[i]))) return FOS_ERR_INVALID_ARG;
+        if (!empty && (!aligned(x[i], 32) || !aligned(out[i], 32))) return FOS_ERR_MISALIGNED;
+    }
+    int dev = -1;
+    for (int i = 0; i < n; ++i) {
+        const bool empty = rows[i] == 0 || cols[i] == 0;
+        const int d = empty ? common_device({amax[i]}) : common_device({x[i], out[i], amax[i]});
+        if (d < 0 || (dev >= 0 && d != dev)) return FOS_ERR_INVALID_ARG;
+        dev = d;
+    }
+    DeviceScope scope(dev);
+    if (scope.st) return scope.st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (!cfg->amax_is_input) {
+        for (int i = 0; i < n; ++i) {
+            st = cuda_status(run_amax(x[i], dt, rows[i], cols[i], Src::TENSOR, amax[i], nullptr,
+                                      0, s));
+            if (st) return st;
+        }
+    }
+    const Err em = err_of(cfg);
+    const In it = in_of(dt);
+    for (int base = 0; base < n; base += kQdqMaxList) {
+        const int m = (n - base < kQdqMaxList) ? n - base : kQdqMaxList;
+        QdqArgs a;
+        std::memset(&a, 0, sizeof(a));
+        a.n = m;
+        a.six_bound = 6.0f * (float)cfg->e4m3_bound;
+        a.neg_zero = -0.0f;
+        int64_t u = 0;
+        for (int i = 0; i < m; ++i) {
+            QdqTensor& t = a.t[i];
+            t.x = x[base + i];
+            t.out = out[base + i];
+            t.amax = amax[base + i];
+            t.nblk = rows[base + i] * (cols[base + i] / 16);
+            t.unit_begin = u;
+            u += (t.nblk + 31) / 32;
+        }
+        a.t[m].unit_begin = u;
+        a.units = u;
+        if (u == 0) continue;
+        st = cuda_status(launch_qdq(it, em, a, s));
+        if (st) return st;
+    }
+    return FOS_OK;
+}
+
+fos_status fos_diag_convert(int op, const void* in, void* out, int64_t n, fos_stream_t stream) {
+    if (op < FOS_DIAG_E2M1_ENCODE || op > FOS_DIAG_DIV6) return FOS_ERR_INVALID_ARG;
+    if (n < 0) return FOS_ERR_INVALID_ARG;
+    if (n == 0) return FOS_OK;
+    if (!in || !out) return FOS_ERR_INVALID_ARG;
+    const int dev = common_device({in, out});
+    if (dev < 0) return FOS_ERR_INVALID_ARG;
+    DeviceScope scope(dev);
+    if (scope.st) return scope.st;
+    return cuda_status(launch_diag(op, in, out, n, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

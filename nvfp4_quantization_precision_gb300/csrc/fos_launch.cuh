@@ -1,0 +1,79 @@
+// fos_launch.cuh -- host-side launch helpers shared by the kernel
+// translation units: persistent grid sizing and the per-family launchers.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <mutex>
+#include <unordered_map>
+
+#include "fos_kernels.cuh"
+
+namespace fos {
+
+// Number of SMs of the current device (cached per device).
+inline int sm_count() {
+    static std::mutex mu;
+    static std::unordered_map<int, int> cache;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    std::lock_guard<std::mutex> g(mu);
+    auto it = cache.find(dev);
+    if (it != cache.end()) return it->second;
+    int n = 1;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    cache[dev] = n > 0 ? n : 1;
+    return cache[dev];
+}
+
+// Persistent grid: as many CTAs as stay resident (SMs x occupancy), but no
+// more than one warp per work unit needs.
+template <class Kernel>
+inline int persistent_grid(Kernel kernel, int64_t units, size_t dyn_smem) {
+    int occ = 1;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, kThreads, dyn_smem) !=
+            cudaSuccess || occ < 1)
+        occ = 1;
+    const int64_t full = (int64_t)sm_count() * occ;
+    const int64_t need = (units + kWarps - 1) / kWarps;
+    int64_t g = need < full ? need : full;
+    return (int)(g < 1 ? 1 : g);
+}
+
+// Raises a kernel's dynamic shared-memory limit when it needs more than the
+// default 48 KiB (once per kernel and size).
+inline cudaError_t allow_smem(const void* kernel, size_t bytes) {
+    if (bytes <= 48 * 1024) return cudaSuccess;
+    static std::mutex mu;
+    static std::unordered_map<const void*, size_t> done;
+    std::lock_guard<std::mutex> g(mu);
+    auto it = done.find(kernel);
+    if (it != done.end() && it->second >= bytes) return cudaSuccess;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)bytes);
+    if (e == cudaSuccess) done[kernel] = bytes;
+    return e;
+}
+
+template <class Kernel, class Args>
+inline cudaError_t launch_persistent(Kernel kernel, const Args& a, int64_t units, size_t dyn_smem,
+                                     cudaStream_t s) {
+    cudaError_t e = allow_smem(reinterpret_cast<const void*>(kernel), dyn_smem);
+    if (e != cudaSuccess) return e;
+    const int grid = persistent_grid(kernel, units, dyn_smem);
+    kernel<<<grid, kThreads, dyn_smem, s>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quant1x16_bf16(Err, Src, const EncArgs&, cudaStream_t);
+cudaError_t launch_quant1x16_f16(Err, Src, const EncArgs&, cudaStream_t);
+cudaError_t launch_quant1x16_f32(Err, Src, const EncArgs&, cudaStream_t);
+cudaError_t launch_quant16x16_bf16(Err, Src, const EncArgs&, cudaStream_t);
+cudaError_t launch_quant16x16_f16(Err, Src, const EncArgs&, cudaStream_t);
+cudaError_t launch_quant16x16_f32(Err, Src, const EncArgs&, cudaStream_t);
+cudaError_t launch_qdq(In, Err, const QdqArgs&, cudaStream_t);
+cudaError_t launch_dequant(Out, bool b16, Src, const DeqArgs&, cudaStream_t);
+cudaError_t launch_amax(In, Src, const AmaxArgs&, cudaStream_t);
+cudaError_t launch_diag(int op, const void* in, void* out, int64_t n, cudaStream_t);
+
+}  // namespace fos

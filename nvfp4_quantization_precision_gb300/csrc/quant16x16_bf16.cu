@@ -1,0 +1,34 @@
+// Instantiations of the 16x16 quantize kernel for bf16 input.
+#include "fos_launch.cuh"
+
+namespace fos {
+
+template <Err EM, Src SRC>
+static cudaError_t go(const EncArgs& a, cudaStream_t s) {
+    const size_t dyn = ring_smem_bytes<In::BF16>() +
+                       ((SRC == Src::GROUP) ? sizeof(int32_t) * (size_t)a.G : 0);
+    return launch_persistent(k_quant16x16<In::BF16, EM, SRC>, a, a.units, dyn, s);
+}
+
+template <Err EM>
+static cudaError_t by_src(Src src, const EncArgs& a, cudaStream_t s) {
+    switch (src) {
+        case Src::TENSOR: return go<EM, Src::TENSOR>(a, s);
+        case Src::ROW: return go<EM, Src::ROW>(a, s);
+        case Src::GROUP: return go<EM, Src::GROUP>(a, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_quant16x16_bf16(Err em, Src src, const EncArgs& a, cudaStream_t s) {
+    switch (em) {
+        case Err::STD: return by_src<Err::STD>(src, a, s);
+        case Err::MAE: return by_src<Err::MAE>(src, a, s);
+        case Err::MSE: return by_src<Err::MSE>(src, a, s);
+        case Err::MAE_H: return by_src<Err::MAE_H>(src, a, s);
+        case Err::MSE_H: return by_src<Err::MSE_H>(src, a, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace fos

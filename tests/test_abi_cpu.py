@@ -1,0 +1,147 @@
+"""C-ABI library checks that need no GPU: it builds, loads, exports every
+function the public headers declare, and rejects bad arguments on the host
+before touching the CUDA runtime."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import nvfp4_quantization_precision_gb300 as fos
+from nvfp4_quantization_precision_gb300 import build as fos_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    fos_build.build()
+    return fos.lib()
+
+
+def _declared():
+    names = set()
+    for h in ("fos.h", "fos_diag.h"):
+        src = open(os.path.join(ROOT, "include", h)).read()
+        names |= set(re.findall(r"FOS_API\s+[\w\s\*]+?\b(fos_\w+)\s*\(", src))
+    return names
+
+
+def test_headers_declare_the_entry_points():
+    d = _declared()
+    for n in ("fos_amax", "fos_quantize", "fos_dequantize", "fos_qdq", "fos_quantize_grouped",
+              "fos_status_string", "fos_version", "fos_diag_convert"):
+        assert n in d
+
+
+def test_library_exports_every_declared_symbol(L):
+    for n in _declared():
+        assert hasattr(L, n), n
+    # nothing else leaks out of the library's C namespace
+    out = os.popen("nm -D --defined-only %s" % fos.LIB_PATH).read()
+    exported = set(re.findall(r" T (fos_\w+)", out))
+    assert exported == _declared()
+
+
+def test_status_strings(L):
+    assert fos.status_string(fos.FOS_OK) == "ok"
+    assert "misaligned" in fos.status_string(fos.FOS_ERR_MISALIGNED)
+    assert L.fos_version() == 10000
+
+
+def _cfg(**kw):
+    base = dict(block=0, mode=1, err_metric=1, err_precision=0, e4m3_bound=448, granularity=0,
+                amax_is_input=1)
+    base.update(kw)
+    return fos.FosConfig(**base)
+
+
+FAKE = ctypes.c_void_p(0x10000)  # never dereferenced: every call below fails validation
+
+
+@pytest.mark.parametrize("kw,rc", [
+    (dict(block=2), fos.FOS_ERR_INVALID_ARG),
+    (dict(mode=7), fos.FOS_ERR_INVALID_ARG),
+    (dict(err_metric=-1), fos.FOS_ERR_INVALID_ARG),
+    (dict(err_precision=3), fos.FOS_ERR_INVALID_ARG),
+    (dict(granularity=2), fos.FOS_ERR_INVALID_ARG),
+    (dict(amax_is_input=5), fos.FOS_ERR_INVALID_ARG),
+    (dict(e4m3_bound=300), fos.FOS_ERR_UNSUPPORTED),
+])
+def test_quantize_rejects_bad_config(L, kw, rc):
+    c = _cfg(**kw)
+    assert L.fos_quantize(FAKE, 0, 16, 16, ctypes.byref(c), FAKE, FAKE, FAKE, None) == rc
+
+
+@pytest.mark.parametrize("rows,cols,block,rc", [
+    (-1, 16, 0, fos.FOS_ERR_INVALID_ARG),
+    (16, -16, 0, fos.FOS_ERR_INVALID_ARG),
+    (16, 24, 0, fos.FOS_ERR_UNSUPPORTED),
+    (8, 16, 1, fos.FOS_ERR_UNSUPPORTED),
+    (1 << 40, 1 << 20, 0, fos.FOS_ERR_UNSUPPORTED),
+])
+def test_quantize_rejects_bad_shape(L, rows, cols, block, rc):
+    c = _cfg(block=block)
+    assert L.fos_quantize(FAKE, 0, rows, cols, ctypes.byref(c), FAKE, FAKE, FAKE, None) == rc
+
+
+def test_quantize_rejects_null_and_misaligned(L):
+    c = _cfg()
+    assert L.fos_quantize(None, 0, 16, 16, ctypes.byref(c), FAKE, FAKE, FAKE, None) == \
+        fos.FOS_ERR_INVALID_ARG
+    assert L.fos_quantize(FAKE, 9, 16, 16, ctypes.byref(c), FAKE, FAKE, FAKE, None) == \
+        fos.FOS_ERR_INVALID_ARG
+    assert L.fos_quantize(ctypes.c_void_p(0x10010), 0, 16, 16, ctypes.byref(c), FAKE, FAKE, FAKE,
+                          None) == fos.FOS_ERR_MISALIGNED
+    assert L.fos_quantize(FAKE, 0, 16, 16, ctypes.byref(c), FAKE, ctypes.c_void_p(0x10004), FAKE,
+                          None) == fos.FOS_ERR_MISALIGNED
+    assert L.fos_quantize(FAKE, 0, 16, 16, None, FAKE, FAKE, FAKE, None) == fos.FOS_ERR_INVALID_ARG
+
+
+def test_grouped_rejects_bad_groups(L):
+    c = _cfg()
+    args = (FAKE, 0, 64, 64, FAKE)
+    assert L.fos_quantize_grouped(*args, 0, ctypes.byref(c), FAKE, FAKE, FAKE, None) == \
+        fos.FOS_ERR_INVALID_ARG
+    assert L.fos_quantize_grouped(*args, fos.GROUPED_MAX_GROUPS + 1, ctypes.byref(c), FAKE, FAKE,
+                                  FAKE, None) == fos.FOS_ERR_UNSUPPORTED
+    assert L.fos_quantize_grouped(FAKE, 0, 64, 64, ctypes.c_void_p(0x10002), 4, ctypes.byref(c),
+                                  FAKE, FAKE, FAKE, None) == fos.FOS_ERR_MISALIGNED
+
+
+def test_qdq_rejects_unsupported(L):
+    P = ctypes.c_void_p * 1
+    xs, outs, am = P(FAKE.value), P(FAKE.value), P(FAKE.value)
+    rows = (ctypes.c_int64 * 1)(16)
+    cols = (ctypes.c_int64 * 1)(16)
+    for kw in (dict(block=1), dict(granularity=1)):
+        c = _cfg(**kw)
+        assert L.fos_qdq(1, xs, outs, rows, cols, am, 0, ctypes.byref(c), None) == \
+            fos.FOS_ERR_UNSUPPORTED
+    c = _cfg()
+    assert L.fos_qdq(1, xs, outs, rows, cols, am, 2, ctypes.byref(c), None) == \
+        fos.FOS_ERR_UNSUPPORTED  # fp32 fused QDQ is not offered
+    assert L.fos_qdq(-1, xs, outs, rows, cols, am, 0, ctypes.byref(c), None) == \
+        fos.FOS_ERR_INVALID_ARG
+    assert L.fos_qdq(0, None, None, None, None, None, 0, ctypes.byref(c), None) == fos.FOS_OK
+    bad = (ctypes.c_int64 * 1)(24)
+    assert L.fos_qdq(1, xs, outs, rows, bad, am, 0, ctypes.byref(c), None) == \
+        fos.FOS_ERR_UNSUPPORTED
+
+
+def test_dequantize_and_amax_and_diag_reject(L):
+    c = _cfg()
+    assert L.fos_dequantize(FAKE, FAKE, FAKE, 16, 16, ctypes.byref(c), FAKE, 7, None) == \
+        fos.FOS_ERR_INVALID_ARG
+    assert L.fos_dequantize(FAKE, FAKE, FAKE, 16, 16, ctypes.byref(c), ctypes.c_void_p(0x10008),
+                            0, None) == fos.FOS_ERR_MISALIGNED
+    assert L.fos_amax(FAKE, 0, 16, 16, 3, FAKE, None) == fos.FOS_ERR_INVALID_ARG
+    assert L.fos_amax(FAKE, 0, 16, 17, 0, FAKE, None) == fos.FOS_ERR_UNSUPPORTED
+    assert L.fos_diag_convert(99, FAKE, FAKE, 4, None) == fos.FOS_ERR_INVALID_ARG
+    assert L.fos_diag_convert(0, FAKE, FAKE, 0, None) == fos.FOS_OK
+
+
+def test_python_binding_refuses_cpu_tensors():
+    import torch
+    with pytest.raises(ValueError):
+        fos.quantize(torch.zeros(16, 16, dtype=torch.bfloat16))

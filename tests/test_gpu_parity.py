@@ -1,0 +1,420 @@
+"""GPU parity: the CUDA library (through its C ABI) against the CPU oracle on
+identical seeded bytes.  Tolerance 0 everywhere: codes, scales, amax and
+outputs are compared as integer views, so signed zeros and NaN payloads of
+the outputs count."""
+import itertools
+
+import numpy as np
+import pytest
+import torch
+
+import nvfp4_quantization_precision_gb300 as fos
+import oracle
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+DTYPES = {"bf16": torch.bfloat16, "f16": torch.float16, "f32": torch.float32}
+MODES = {  # name -> (four_over_six, mse, err_f16)
+    "std": (False, True, False),
+    "mae": (True, False, False),
+    "mse": (True, True, False),
+    "mae_f16": (True, False, True),
+    "mse_f16": (True, True, True),
+}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+    __graft_entry__.build()
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+
+
+def _cfgs(mode, bound=448, row=False, b16=False):
+    f, m, h = MODES[mode]
+    return (fos.Config(block16x16=b16, four_over_six=f, mse=m, err_f16=h, bound=bound,
+                       row_scaled=row),
+            oracle.Config(block16x16=b16, four_over_six=f, mse=m, err_f16=h, bound=bound,
+                          row_scaled=row))
+
+
+def _u16(t):
+    return t.cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def _u32(t):
+    return t.cpu().contiguous().view(torch.int32).numpy().view(np.uint32)
+
+
+def _x(rows, cols, fam, seed, dt):
+    return workloads.activation(rows, cols, fam, seed=seed, dtype=DTYPES[dt])
+
+
+def _check_quant(x, gcfg, ocfg, amax_given):
+    """Run both sides; amax either computed by each side or given (oracle's)."""
+    xf = x.float().numpy()
+    if amax_given:
+        a = oracle.amax_rows(xf) if ocfg.row_scaled else oracle.amax_tensor(xf)
+        ocfg = oracle.Config(**{**ocfg.__dict__, "amax_is_input": True})
+        oc, os_, oa = oracle.quantize(xf, ocfg, amax=a)
+        gc, gs, ga = fos.quantize(x.to(DEV), gcfg, amax=torch.from_numpy(a).to(DEV))
+    else:
+        oc, os_, oa = oracle.quantize(xf, ocfg)
+        gc, gs, ga = fos.quantize(x.to(DEV), gcfg)
+    torch.cuda.synchronize()
+    assert np.array_equal(_u32(ga), oa.view(np.uint32)), "amax"
+    gcn, gsn = gc.cpu().numpy(), gs.cpu().numpy()
+    if not np.array_equal(gsn, os_):
+        bad = np.argwhere(gsn != os_)
+        raise AssertionError("scales differ at %d places, first %s: gpu %#x oracle %#x" % (
+            len(bad), bad[0], gsn[tuple(bad[0])], os_[tuple(bad[0])]))
+    if not np.array_equal(gcn, oc):
+        bad = np.argwhere(gcn != oc)
+        raise AssertionError("codes differ at %d places, first %s" % (len(bad), bad[0]))
+    return gc, gs, ga
+
+
+# ------------------------------------------------------------------ 1x16
+@pytest.mark.parametrize("dt,mode,bound,row", list(itertools.product(
+    ["bf16", "f16", "f32"], list(MODES), [448, 256], [False, True])))
+def test_quantize_1x16_knobs(dt, mode, bound, row):
+    gcfg, ocfg = _cfgs(mode, bound, row)
+    for i, (fam, shape) in enumerate(zip(workloads.FAMILIES,
+                                         [(256, 1024), (48, 272), (7, 1040), (33, 528)])):
+        x = _x(*shape, fam, seed=i, dt=dt)
+        _check_quant(x, gcfg, ocfg, amax_given=(i % 2 == 1))
+
+
+@pytest.mark.parametrize("shape", [(1, 16), (3, 16), (1, 512), (5, 496), (2, 8192), (129, 32)])
+def test_quantize_1x16_ragged_shapes(shape):
+    for mode in ("std", "mse", "mae_f16"):
+        for row in (False, True):
+            gcfg, ocfg = _cfgs(mode, 448, row)
+            _check_quant(_x(*shape, "F4", 3, "bf16"), gcfg, ocfg, amax_given=False)
+
+
+def test_quantize_pr1_config():
+    # one 256x1024 bf16 tensor, N(0,1), per-tensor amax, E4M3 448, MSE exact
+    gcfg, ocfg = _cfgs("mse", 448, False)
+    for seed in (0, 1, 2):
+        _check_quant(_x(256, 1024, "F1", seed, "bf16"), gcfg, ocfg, amax_given=False)
+
+
+# ------------------------------------------------------------------ 16x16
+@pytest.mark.parametrize("dt,mode,bound,row", list(itertools.product(
+    ["bf16", "f16", "f32"], list(MODES), [448, 256], [False, True])))
+def test_quantize_16x16_knobs(dt, mode, bound, row):
+    gcfg, ocfg = _cfgs(mode, bound, row, b16=True)
+    for i, shape in enumerate([(64, 272), (32, 1024), (16, 16)]):
+        x = workloads.weight(*shape, seed=i, dtype=DTYPES[dt])
+        if row:  # per-row amax made tile-uniform (the contract for 16x16)
+            xf = x.float().numpy()
+            a = np.repeat(oracle.amax_rows(xf).reshape(-1, 16).max(1), 16)
+            ocfg2 = oracle.Config(**{**ocfg.__dict__, "amax_is_input": True})
+            oc, os_, _ = oracle.quantize(xf, ocfg2, amax=a)
+            gc, gs, _ = fos.quantize(x.to(DEV), gcfg, amax=torch.from_numpy(a).to(DEV))
+            torch.cuda.synchronize()
+            assert np.array_equal(gs.cpu().numpy(), os_)
+            assert np.array_equal(gc.cpu().numpy(), oc)
+        else:
+            _check_quant(x, gcfg, ocfg, amax_given=(i == 1))
+
+
+def test_16x16_row_amax_uses_first_tile_row():
+    # non-uniform per-row amax: every tile takes its first row's value
+    x = workloads.weight(64, 256, seed=5, dtype=torch.bfloat16)
+    xf = x.float().numpy()
+    a = oracle.amax_rows(xf)
+    gcfg, ocfg = _cfgs("mse", 448, True, b16=True)
+    ocfg = oracle.Config(**{**ocfg.__dict__, "amax_is_input": True})
+    oc, os_, _ = oracle.quantize(xf, ocfg, amax=a)
+    gc, gs, _ = fos.quantize(x.to(DEV), gcfg, amax=torch.from_numpy(a).to(DEV))
+    torch.cuda.synchronize()
+    assert np.array_equal(gs.cpu().numpy(), os_) and np.array_equal(gc.cpu().numpy(), oc)
+
+
+# ------------------------------------------------------------------ special values
+def _special_tensor(dt):
+    rng = np.random.default_rng(0)
+    x = rng.standard_normal((64, 64)).astype(np.float32)
+    x[0, :16] = np.nan                     # all-NaN block
+    x[1, 3] = np.nan                       # one NaN
+    x[2, 0] = np.inf
+    x[3, 5] = -np.inf
+    x[4, :16] = 0.0
+    x[5, :16] = -0.0
+    x[6, :16] *= 1e-7                      # scale underflows E4M3
+    x[7, :16] = np.float32(2.0 ** -130)    # subnormal f32 (bf16 keeps it)
+    x[8, :16] = 6.0                        # exact grid values
+    x[9, :16] = np.array([0.5, 1, 1.5, 2, 3, 4, 6, 0] * 2, np.float32)
+    x[10, :] = 1e30 if dt != "f16" else 6e4
+    x[11, 16:32] = -x[11, 16:32]
+    return torch.from_numpy(x).to(DTYPES[dt])
+
+
+@pytest.mark.parametrize("dt", ["bf16", "f16", "f32"])
+@pytest.mark.parametrize("mode", list(MODES))
+@pytest.mark.parametrize("row", [False, True])
+def test_special_values(dt, mode, row):
+    gcfg, ocfg = _cfgs(mode, 448, row)
+    _check_quant(_special_tensor(dt), gcfg, ocfg, amax_given=False)
+    # the same rows with amax given as extreme values
+    x = _special_tensor(dt)
+    n = x.shape[0] if row else 1
+    for aval in (0.0, float("inf"), 1e-38, 3e38, float("nan"), -1.0):
+        a = np.full(n, aval, np.float32)
+        ocfg2 = oracle.Config(**{**ocfg.__dict__, "amax_is_input": True})
+        oc, os_, _ = oracle.quantize(x.float().numpy(), ocfg2, amax=a)
+        gc, gs, _ = fos.quantize(x.to(DEV), gcfg, amax=torch.from_numpy(a).to(DEV))
+        torch.cuda.synchronize()
+        assert np.array_equal(gs.cpu().numpy(), os_), aval
+        assert np.array_equal(gc.cpu().numpy(), oc), aval
+
+
+# ------------------------------------------------------------------ dequantize
+@pytest.mark.parametrize("out", ["bf16", "f16", "f32"])
+@pytest.mark.parametrize("b16", [False, True])
+@pytest.mark.parametrize("row", [False, True])
+def test_dequantize(out, b16, row):
+    rng = np.random.default_rng(3)
+    R, C = 48, 272
+    codes = rng.integers(0, 256, (R, C // 2), dtype=np.uint8)
+    srows = R // 16 if b16 else R
+    scales = rng.integers(0, 0x7F, (srows, C // 16), dtype=np.uint8)
+    a = rng.uniform(0.01, 100, R if row else 1).astype(np.float32)
+    if row and b16:
+        a = np.repeat(a[::16], 16)
+    ocfg = oracle.Config(block16x16=b16, row_scaled=row, bound=256)
+    gcfg = fos.Config(block16x16=b16, row_scaled=row, bound=256)
+    ref = oracle.dequantize(codes, scales, a, ocfg, out)
+    got = fos.dequantize(torch.from_numpy(codes).to(DEV), torch.from_numpy(scales).to(DEV),
+                         torch.from_numpy(a).to(DEV), gcfg, out_dtype=DTYPES[out])
+    torch.cuda.synchronize()
+    g = _u32(got) if out == "f32" else _u16(got)
+    assert np.array_equal(g, ref.view(g.dtype))
+
+
+def test_dequantize_all_scale_codes():
+    codes = np.tile(np.arange(256, dtype=np.uint8).reshape(1, 256)[:, :8], (256, 1))
+    scales = np.arange(256, dtype=np.uint8).reshape(256, 1)
+    a = np.array([7.0], np.float32)
+    ocfg, gcfg = oracle.Config(), fos.Config()
+    ref = oracle.dequantize(codes, scales, a, ocfg, "f32")
+    got = fos.dequantize(torch.from_numpy(codes).to(DEV), torch.from_numpy(scales).to(DEV),
+                         torch.from_numpy(a).to(DEV), gcfg, out_dtype=torch.float32).cpu().numpy()
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan].view(np.uint32), ref[~nan].view(np.uint32))
+
+
+# ------------------------------------------------------------------ fused QDQ
+@pytest.mark.parametrize("dt", ["bf16", "f16"])
+@pytest.mark.parametrize("mode", list(MODES))
+@pytest.mark.parametrize("bound", [448, 256])
+def test_qdq_list(dt, mode, bound):
+    gcfg, ocfg = _cfgs(mode, bound)
+    shapes = [(64, 1024), (0, 64), (7, 1040), (48, 272), (1, 16)]
+    xs = [workloads.qdq_weights(1, r, c, seed=i, dtype=DTYPES[dt])[0] if r else
+          torch.zeros(0, c, dtype=DTYPES[dt]) for i, (r, c) in enumerate(shapes)]
+    outs = fos.qdq([x.to(DEV) for x in xs], gcfg)
+    torch.cuda.synchronize()
+    for x, o in zip(xs, outs):
+        if x.numel() == 0:
+            continue
+        ref, _ = oracle.qdq(x.float().numpy(), ocfg, dt)
+        assert np.array_equal(_u16(o), ref)
+
+
+def test_qdq_equals_dequantize_of_quantize_on_gpu():
+    gcfg, _ = _cfgs("mse_f16", 256)
+    x = workloads.qdq_weights(1, 128, 7168, seed=4)[0].to(DEV)
+    a = fos.amax(x)
+    q = fos.qdq([x], gcfg, amaxes=[a])[0]
+    c, s, _ = fos.quantize(x, gcfg, amax=a)
+    d = fos.dequantize(c, s, a, gcfg, out_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    assert torch.equal(q.view(torch.int16), d.view(torch.int16))
+
+
+def test_qdq_long_list_splits_launches():
+    gcfg, ocfg = _cfgs("mae", 448)
+    xs = [workloads.qdq_weights(1, 2, 32, seed=i)[0] for i in range(fos.QDQ_MAX_LIST + 5)]
+    outs = fos.qdq([x.to(DEV) for x in xs], gcfg)
+    torch.cuda.synchronize()
+    for x, o in zip(xs, outs):
+        ref, _ = oracle.qdq(x.float().numpy(), ocfg, "bf16")
+        assert np.array_equal(_u16(o), ref)
+
+
+# ------------------------------------------------------------------ grouped
+@pytest.mark.parametrize("b16", [False, True])
+@pytest.mark.parametrize("dt", ["bf16", "f32"])
+@pytest.mark.parametrize("mode", ["std", "mse", "mae_f16"])
+@pytest.mark.parametrize("given", [False, True])
+def test_grouped(b16, dt, mode, given):
+    R, C = 512, 272
+    offs = workloads.moe_offsets(R, 12, seed=1, n_empty=3, multiple=16 if b16 else 1)
+    x = workloads.moe_activations(R, C, offs, seed=2, dtype=DTYPES[dt])
+    gcfg, ocfg = _cfgs(mode, 448, b16=b16)
+    xf = x.float().numpy()
+    on = offs.numpy()
+    if given:
+        ga_in = oracle.amax_groups(xf, on)
+        ocfg = oracle.Config(**{**ocfg.__dict__, "amax_is_input": True})
+        oc, os_, oa = oracle.quantize_grouped(xf, on, ocfg, group_amax=ga_in)
+        gc, gs, ga = fos.quantize_grouped(x.to(DEV), offs.to(DEV), gcfg,
+                                          group_amax=torch.from_numpy(ga_in).to(DEV))
+    else:
+        oc, os_, oa = oracle.quantize_grouped(xf, on, ocfg)
+        gc, gs, ga = fos.quantize_grouped(x.to(DEV), offs.to(DEV), gcfg)
+    torch.cuda.synchronize()
+    assert np.array_equal(_u32(ga), oa.view(np.uint32))
+    assert np.array_equal(gs.cpu().numpy(), os_)
+    assert np.array_equal(gc.cpu().numpy(), oc)
+
+
+def test_grouped_bad_offs_are_clamped_like_the_oracle():
+    R, C = 64, 64
+    x = _x(R, C, "F1", 9, "bf16")
+    offs = np.array([10, 5, 40, 200, 30], np.int32)  # non-monotone and past the end
+    gcfg, ocfg = _cfgs("mse")
+    oc, os_, oa = oracle.quantize_grouped(x.float().numpy(), offs, ocfg)
+    gc, gs, ga = fos.quantize_grouped(x.to(DEV), torch.from_numpy(offs).to(DEV), gcfg)
+    torch.cuda.synchronize()
+    assert np.array_equal(_u32(ga), oa.view(np.uint32))
+    assert np.array_equal(gs.cpu().numpy(), os_) and np.array_equal(gc.cpu().numpy(), oc)
+
+
+def test_grouped_equals_per_group_gpu_calls():
+    R, C = 1024, 512
+    offs = workloads.moe_offsets(R, 16, seed=3)
+    x = workloads.moe_activations(R, C, offs, seed=4).to(DEV)
+    gcfg, _ = _cfgs("mse")
+    gc, gs, ga = fos.quantize_grouped(x, offs.to(DEV), gcfg)
+    lo = 0
+    for g, hi in enumerate(offs.tolist()):
+        if hi > lo:
+            c, s, a = fos.quantize(x[lo:hi].contiguous(), gcfg)
+            torch.cuda.synchronize()
+            assert torch.equal(a[0], ga[g])
+            assert torch.equal(c, gc[lo:hi]) and torch.equal(s, gs[lo:hi])
+        lo = hi
+    assert bool((gc[lo:] == 0).all()) and bool((gs[lo:] == 0).all())
+
+
+# ------------------------------------------------------------------ amax
+@pytest.mark.parametrize("dt", ["bf16", "f16", "f32"])
+def test_amax(dt):
+    x = _special_tensor(dt)
+    xf = x.float().numpy()
+    g = fos.amax(x.to(DEV))
+    r = fos.amax(x.to(DEV), row_scaled=True)
+    torch.cuda.synchronize()
+    assert np.array_equal(_u32(g), oracle.amax_tensor(xf).view(np.uint32))
+    assert np.array_equal(_u32(r), oracle.amax_rows(xf).view(np.uint32))
+
+
+# ------------------------------------------------------------------ primitives
+def _dense_f32(n_random=1 << 22, seed=0):
+    rng = np.random.default_rng(seed)
+    top = (np.arange(0, 1 << 16, dtype=np.uint32) << 16)
+    lows = np.array([0, 1, 0x7FFF, 0x8000, 0x8001, 0xFFFF], np.uint32)
+    dense = (top[:, None] | lows[None, :]).ravel()
+    rand = rng.integers(0, 1 << 32, n_random, dtype=np.uint64).astype(np.uint32)
+    return np.concatenate([dense, rand]).view(np.float32)
+
+
+def _run_diag(op, arr, out_dtype):
+    inp = torch.from_numpy(arr).to(DEV)
+    out = torch.empty(arr.size, dtype=out_dtype, device=DEV)
+    fos.diag_convert(op, inp, out)
+    torch.cuda.synchronize()
+    return out.cpu()
+
+
+def test_diag_e2m1_encode_matches_oracle():
+    v = _dense_f32()
+    got = _run_diag(fos.DIAG_E2M1_ENCODE, v, torch.uint8).numpy()
+    ref = oracle.e2m1_encode(v)
+    bad = np.nonzero(got != ref)[0]
+    assert bad.size == 0, [(hex(v.view(np.uint32)[i]), hex(got[i]), hex(ref[i])) for i in bad[:8]]
+
+
+def test_diag_e2m1_decode_all_codes():
+    codes = np.arange(16, dtype=np.uint8)
+    got = _run_diag(fos.DIAG_E2M1_DECODE, codes, torch.float32).numpy()
+    ref = np.array([oracle.e2m1_value(c) for c in range(16)], np.float32)
+    assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
+
+
+def test_diag_e4m3_encode_matches_oracle():
+    v = _dense_f32(1 << 20, seed=1)
+    got = _run_diag(fos.DIAG_E4M3_ENCODE, v, torch.uint8).numpy()
+    ref = oracle.e4m3_encode(v)
+    nan = np.isnan(v)
+    # NaN inputs never reach the E4M3 cast on the quantize path; compare NaN-ness only
+    assert ((got[nan] & 0x7F) == 0x7F).all()
+    bad = np.nonzero((got != ref) & ~nan)[0]
+    assert bad.size == 0, [(float(v[i]), hex(got[i]), hex(ref[i])) for i in bad[:8]]
+
+
+def test_diag_e4m3_decode_all_codes():
+    codes = np.arange(256, dtype=np.uint8)
+    got = _run_diag(fos.DIAG_E4M3_DECODE, codes, torch.float32).numpy()
+    ref = np.array([oracle.e4m3_value(c) for c in range(256)], np.float32)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan].view(np.uint32), ref[~nan].view(np.uint32))
+
+
+def test_diag_f16_and_bf16_rounding():
+    v = _dense_f32(1 << 20, seed=2)
+    v = v[~np.isnan(v)]
+    v = v[: v.size // 2 * 2]
+    got = _run_diag(fos.DIAG_F16_ROUND, v, torch.float32).numpy()
+    assert np.array_equal(got.view(np.uint32), oracle.f16_round(v).view(np.uint32))
+    got = _run_diag(fos.DIAG_F16_BITS, v, torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(got, oracle.f16_bits(v))
+    got = _run_diag(fos.DIAG_BF16_BITS, v, torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(got, oracle.bf16_bits(v))
+
+
+def test_diag_div6_is_correctly_rounded():
+    v = _dense_f32(1 << 22, seed=3)
+    got = _run_diag(fos.DIAG_DIV6, v, torch.float32).numpy()
+    with np.errstate(all="ignore"):
+        ref = (v / np.float32(6.0)).astype(np.float32)  # IEEE binary32 division
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan].view(np.uint32), ref[~nan].view(np.uint32))
+
+
+# ------------------------------------------------------------------ full size
+def test_activation_full_size_sampled():
+    """8192x4096 bf16, per-tensor amax computed on the device, launched exactly
+    as the benchmark launches it; the oracle checks a sample of rows (the
+    global amax and therefore S come from the whole tensor)."""
+    gen_dev = torch.device(DEV)
+    for fam in workloads.FAMILIES:
+        x = workloads.activation(8192, 4096, fam, seed=0, dtype=torch.bfloat16, device=gen_dev)
+        for mode in ("mse", "mae_f16", "std"):
+            for row in (False, True):
+                gcfg, ocfg = _cfgs(mode, 448 if mode != "mae_f16" else 256, row)
+                gc, gs, ga = fos.quantize(x, gcfg)
+                torch.cuda.synchronize()
+                xs = x.cpu()
+                rows = np.random.default_rng(5).choice(8192, 48, replace=False)
+                if row:
+                    ref_a = oracle.amax_rows(xs[rows].float().numpy())
+                    assert np.array_equal(_u32(ga[torch.from_numpy(rows).to(DEV)]),
+                                          ref_a.view(np.uint32))
+                else:
+                    ref_a = oracle.amax_tensor(xs.float().numpy())
+                    assert np.array_equal(_u32(ga), ref_a.view(np.uint32))
+                ocfg2 = oracle.Config(**{**ocfg.__dict__, "amax_is_input": True})
+                oc, os_, _ = oracle.quantize(xs[rows].float().numpy(), ocfg2, amax=ref_a)
+                assert np.array_equal(gc.cpu().numpy()[rows], oc), (fam, mode, row)
+                assert np.array_equal(gs.cpu().numpy()[rows], os_), (fam, mode, row)
