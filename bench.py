@@ -197,6 +197,27 @@ def _time_events(fn, reps, stream):
     return e0.elapsed_time(e1) / reps
 
 
+def _graph(fn):
+    """fn() captured once into a CUDA graph (after one eager call that warms
+    the library's per-kernel caches).  Replaying the graph issues the same
+    C-ABI work with no host time between the kernels."""
+    import torch
+    fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    torch.cuda.synchronize()
+    return g
+
+
+def _graph_ms(fn, reps, stream, replays=5):
+    """Average device time of one fn() from a graph holding `reps` calls."""
+    g = _graph(lambda: [fn() for _ in range(reps)])
+    g.replay()
+    return _time_events(g.replay, replays, stream) / reps
+
+
 # ----------------------------------------------------------------- our arm
 def run_fos(args):
     import torch
@@ -221,33 +242,26 @@ def run_fos(args):
     codes = [torch.empty(ROWS, COLS // 2, dtype=torch.uint8, device=dev) for _ in xs]
     scales = [torch.empty(ROWS, COLS // 16, dtype=torch.uint8, device=dev) for _ in xs]
     cfg = fos.Config(four_over_six=True, mse=True, err_f16=False, bound=448)
-    L = fos.lib()
-    import ctypes
-    cc = cfg.c(True)
-    sp = ctypes.c_void_p(stream.cuda_stream)
-    xp = [ctypes.c_void_p(x.data_ptr()) for x in xs]
-    ap = [ctypes.c_void_p(a.data_ptr()) for a in amax]
-    cp = [ctypes.c_void_p(c.data_ptr()) for c in codes]
-    spp = [ctypes.c_void_p(s.data_ptr()) for s in scales]
-    ev_enc = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(args.steps)]
 
     def amax_phase():
         for i in range(4):
-            rc = L.fos_amax(xp[i], fos.FOS_BF16, ROWS, COLS, 0, ap[i], sp)
-            assert rc == 0, rc
+            fos.amax(xs[i], out=amax[i])
 
     def encode_phase():
         for i in range(4):
-            rc = L.fos_quantize(xp[i], fos.FOS_BF16, ROWS, COLS, ctypes.byref(cc), ap[i], cp[i],
-                                spp[i], sp)
-            assert rc == 0, rc
+            fos.quantize(xs[i], cfg, amax=amax[i], codes=codes[i], scales=scales[i])
+
+    # One step = amax pass of the four tensors, then their encode: two CUDA
+    # graphs of C-ABI calls, replayed back to back.
+    g_amax, g_enc = _graph(amax_phase), _graph(encode_phase)
+    ev_enc = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
 
     def step(k=None):
-        amax_phase()
+        g_amax.replay()
         if k is not None:
             ev_enc[k][0].record(stream)
-        encode_phase()
+        g_enc.replay()
         if k is not None:
             ev_enc[k][1].record(stream)
 
@@ -292,7 +306,7 @@ def run_fos(args):
         "data": "synthetic (seeded families F1-F4, generated on device)",
         "config": {"workload": WORKLOAD, "tensors_per_step_per_gpu": 4,
                    "l2": "inputs larger than L2: 4 x 64 MiB per step, 2x the 129 MB L2",
-                   "bytes_per_tensor": ALG_BYTES},
+                   "bytes_per_tensor": ALG_BYTES, "launch": "CUDA graph replay of C-ABI calls"},
         "pct_of_peak": round(100.0 * value / ws / peak, 2),
         "elements_per_s": round(units * ELEMS / (ms / 1e3), 1),
         "gpu_launches": 8 * args.steps,
@@ -305,8 +319,14 @@ def run_fos(args):
     out["clocks"] = clock_summary
 
     if rank == 0 and ws == 1 and not args.skip_extras:
-        out["e2e"] = _e2e(fos, L, xs, cfg, stream, args)
-        out["rows"] = _rows(fos, L, xs, stream, peak)
+        # the same step issued eagerly (host time between calls included)
+        def eager():
+            amax_phase()
+            encode_phase()
+        eager()
+        out["eager_ms_per_step"] = round(_time_events(eager, max(5, args.steps // 4), stream), 5)
+        out["e2e"] = _e2e(fos, xs, cfg, stream, args)
+        out["rows"] = _rows(fos, xs, stream, peak)
         out["cpu_baseline"] = _cpu_baseline(args.cpu_seconds)
     clocks.stop()
     if ws > 1:
@@ -315,11 +335,10 @@ def run_fos(args):
         print(json.dumps(out))
 
 
-def _e2e(fos, L, xs, cfg, stream, args):
-    """Same step through the C ABI from pinned host buffers: H2D of the four
-    inputs, amax + encode, D2H of codes and scales, all inside the region."""
-    import ctypes
-
+def _e2e(fos, xs, cfg, stream, args):
+    """The step from pinned host buffers through the public API: H2D of the
+    four inputs, amax + encode (fos_quantize computes the amax), D2H of codes
+    and scales, all inside the timed region."""
     import torch
     dev = xs[0].device
     hx = [x.cpu().pin_memory() for x in xs]
@@ -329,17 +348,11 @@ def _e2e(fos, L, xs, cfg, stream, args):
     ds = [torch.empty(ROWS, COLS // 16, dtype=torch.uint8, device=dev) for _ in xs]
     hc = [torch.empty(ROWS, COLS // 2, dtype=torch.uint8).pin_memory() for _ in xs]
     hs = [torch.empty(ROWS, COLS // 16, dtype=torch.uint8).pin_memory() for _ in xs]
-    cc = cfg.c(False)
-    sp = ctypes.c_void_p(stream.cuda_stream)
 
     def step():
         for i in range(4):
             dx[i].copy_(hx[i], non_blocking=True)
-            rc = L.fos_quantize(ctypes.c_void_p(dx[i].data_ptr()), fos.FOS_BF16, ROWS, COLS,
-                                ctypes.byref(cc), ctypes.c_void_p(am[i].data_ptr()),
-                                ctypes.c_void_p(dc[i].data_ptr()),
-                                ctypes.c_void_p(ds[i].data_ptr()), sp)
-            assert rc == 0
+            fos.quantize(dx[i], cfg, amax=am[i], amax_given=False, codes=dc[i], scales=ds[i])
             hc[i].copy_(dc[i], non_blocking=True)
             hs[i].copy_(ds[i], non_blocking=True)
 
@@ -354,110 +367,102 @@ def _e2e(fos, L, xs, cfg, stream, args):
             "steps": reps}
 
 
-def _rows(fos, L, xs, stream, peak):
-    """Kernel-only throughput of every hot-path row at its workload size
-    (inputs rotated over the four tensors, or larger than L2)."""
+def _rows(fos, xs, stream, peak):
+    """Device time of every hot-path row at its workload size, each from a
+    CUDA graph of 8 calls rotating over inputs larger than L2."""
     import torch
 
     import workloads
     dev = xs[0].device
     res = {}
-    reps = 20
+    R8 = 8
     am = [fos.amax(x) for x in xs]
+    ra = [fos.amax(x, row_scaled=True) for x in xs]
     torch.cuda.synchronize()
-    # a1: amax pass
-    ms = _time_events(lambda it=iter(range(10 ** 9)): fos.amax(xs[next(it) % 4], out=am[0]),
-                      reps, stream)
-    res["amax_pass"] = {"GB/s": round(ELEMS * 2 / (ms / 1e3) / 1e9, 1), "ms": round(ms, 5)}
-    # a3-a8: encode sweep, amax given
-    sweep = {}
+
+    def rot(call):
+        it = iter(range(10 ** 9))
+        return lambda: call(next(it) % 4)
+
+    def rec(name, nbytes, ms):
+        res[name] = {"GB/s": round(nbytes / (ms / 1e3) / 1e9, 1), "us": round(ms * 1e3, 2),
+                     "frac": round(nbytes / (ms / 1e3) / 1e9 / peak, 3)}
+
+    # a1: amax pass (reads x once)
+    tmp = torch.zeros(1, dtype=torch.float32, device=dev)
+    rec("amax_pass", ELEMS * 2, _graph_ms(rot(lambda i: fos.amax(xs[i], out=tmp)), R8, stream))
+    # a2-a8: encode sweep, amax given
     codes = torch.empty(ROWS, COLS // 2, dtype=torch.uint8, device=dev)
     scales = torch.empty(ROWS, COLS // 16, dtype=torch.uint8, device=dev)
-    ra = [fos.amax(x, row_scaled=True) for x in xs]
+    sweep = {}
     for four, mse, f16, bound, row in (
             [(False, True, False, 448, False), (False, True, False, 448, True)] +
             [(True, m, h, b, r) for m in (False, True) for h in (False, True)
              for b in (448, 256) for r in (False, True)]):
         c = fos.Config(four_over_six=four, mse=mse, err_f16=f16, bound=bound, row_scaled=row)
-        it = iter(range(10 ** 9))
         a = ra if row else am
-
-        def f():
-            i = next(it) % 4
-            fos.quantize(xs[i], c, amax=a[i], codes=codes, scales=scales)
-        f()
-        ms = _time_events(f, reps, stream)
+        ms = _graph_ms(rot(lambda i: fos.quantize(xs[i], c, amax=a[i], codes=codes,
+                                                  scales=scales)), R8, stream)
         name = ("std" if not four else ("mse" if mse else "mae") + ("_f16" if f16 else "_exact")
                 ) + "_%d_%s" % (bound, "row" if row else "tensor")
         sweep[name] = round(ALG_BYTES / (ms / 1e3) / 1e9, 1)
     res["encode_sweep_GB/s"] = sweep
+    # a1+a8 with the row amax fused?  (row amax is a separate pass; both timed)
+    ms = _graph_ms(rot(lambda i: fos.quantize(xs[i], fos.Config(row_scaled=True),
+                                              codes=codes, scales=scales)), R8, stream)
+    rec("encode_row_scaled_with_amax_pass", ALG_BYTES, ms)
     # a9: fused QDQ at the metric shape and on the 8 x 2048x7168 weight list
-    for label, tensors in (("qdq_8192x4096_bf16", xs),
-                           ("qdq_list_8x2048x7168_bf16",
-                            workloads.qdq_weights(8, 2048, 7168, seed=0, device=dev))):
-        amx = [fos.amax(t) for t in tensors]
-        outs = [torch.empty_like(t) for t in tensors]
-        for mode in ("std", "mse_f16"):
-            c = fos.Config(four_over_six=(mode != "std"), mse=True, err_f16=(mode != "std"))
-            if label.startswith("qdq_list"):
-                def f():
-                    fos.qdq(tensors, c, amaxes=amx, outs=outs)
-                nbytes = sum(t.numel() for t in tensors) * 4
-            else:
-                it = iter(range(10 ** 9))
-
-                def f():
-                    i = next(it) % 4
-                    fos.qdq([tensors[i]], c, amaxes=[amx[i]], outs=[outs[i]])
-                nbytes = ELEMS * 4
-            f()
-            ms = _time_events(f, reps, stream)
-            res["%s_%s" % (label, mode)] = {"GB/s": round(nbytes / (ms / 1e3) / 1e9, 1),
-                                             "ms": round(ms, 5)}
-        del outs
+    outs4 = [torch.empty_like(x) for x in xs]
+    for mode in ("std", "mse_f16", "mse_exact"):
+        c = fos.Config(four_over_six=(mode != "std"), mse=True, err_f16=(mode == "mse_f16"))
+        ms = _graph_ms(rot(lambda i: fos.qdq([xs[i]], c, amaxes=[am[i]], outs=[outs4[i]])),
+                       R8, stream)
+        rec("qdq_8192x4096_bf16_" + mode, ELEMS * 4, ms)
+    del outs4
+    ws_ = workloads.qdq_weights(8, 2048, 7168, seed=0, device=dev)
+    wam = [fos.amax(t) for t in ws_]
+    wout = [torch.empty_like(t) for t in ws_]
+    for mode in ("std", "mse_f16", "mae_f16"):
+        c = fos.Config(four_over_six=(mode != "std"), mse=(mode != "mae_f16"), err_f16=True)
+        ms = _graph_ms(lambda: fos.qdq(ws_, c, amaxes=wam, outs=wout), 2, stream)
+        rec("qdq_list_8x2048x7168_bf16_" + mode, sum(t.numel() for t in ws_) * 4, ms)
+    del ws_, wout
     # a11: dequantize back to bf16
     c = fos.Config()
     cs = [fos.quantize(x, c, amax=a) for x, a in zip(xs, am)]
     out = torch.empty(ROWS, COLS, dtype=torch.bfloat16, device=dev)
-    it = iter(range(10 ** 9))
-
-    def f():
-        i = next(it) % 4
-        fos.dequantize(cs[i][0], cs[i][1], am[i], c, out=out)
-    f()
-    ms = _time_events(f, reps, stream)
-    res["dequantize_bf16"] = {"GB/s": round(ALG_BYTES / (ms / 1e3) / 1e9, 1), "ms": round(ms, 5)}
+    ms = _graph_ms(rot(lambda i: fos.dequantize(cs[i][0], cs[i][1], am[i], c, out=out)), R8,
+                   stream)
+    rec("dequantize_bf16", ALG_BYTES, ms)
     del cs
     # a10: grouped MoE activations, 65536 x 7168 in 64 groups, per-group amax
     R, C = 65536, 7168
-    offs = workloads.moe_offsets(R, 64, seed=0).to(dev)
-    xa = workloads.moe_activations(R, C, offs.cpu(), seed=0, device=dev)
+    offs = workloads.moe_offsets(R, 64, seed=0)
+    xa = workloads.moe_activations(R, C, offs, seed=0, device=dev)
+    offs = offs.to(dev)
     ga = torch.empty(64, dtype=torch.float32, device=dev)
     gc = torch.empty(R, C // 2, dtype=torch.uint8, device=dev)
     gs = torch.empty(R, C // 16, dtype=torch.uint8, device=dev)
     c = fos.Config()
-    fos.quantize_grouped(xa, offs, c, codes=gc, scales=gs)
-    ms = _time_events(lambda: fos.quantize_grouped(xa, offs, c, group_amax=ga, codes=gc,
-                                                   scales=gs), 5, stream)
+    fos.quantize_grouped(xa, offs, c, group_amax=ga, codes=gc, scales=gs)
     live = int(offs[-1].item())
     gbytes = live * C * BYTES_PER_ELEM + (R - live) * C * (0.5 + 1 / 16)
-    res["grouped_moe_65536x7168_amax_given"] = {"GB/s": round(gbytes / (ms / 1e3) / 1e9, 1),
-                                                "ms": round(ms, 4)}
+    ms = _graph_ms(lambda: fos.quantize_grouped(xa, offs, c, group_amax=ga, codes=gc, scales=gs),
+                   2, stream)
+    rec("grouped_moe_65536x7168_amax_given", gbytes, ms)
     del xa, gc, gs
-    # 16x16 weight quantize 14336 x 4096 bf16
-    w = workloads.weight(14336, 4096, seed=0, device=dev)
-    wa = fos.amax(w)
-    c = fos.Config(block16x16=True)
-    wc = torch.empty(14336, 2048, dtype=torch.uint8, device=dev)
-    ws_ = torch.empty(896, 256, dtype=torch.uint8, device=dev)
-    fos.quantize(w, c, amax=wa, codes=wc, scales=ws_)
-    ms = _time_events(lambda: fos.quantize(w, c, amax=wa, codes=wc, scales=ws_), reps, stream)
-    wbytes = 14336 * 4096 * (2 + 0.5 + 1 / 256)
-    res["weight_16x16_14336x4096_bf16"] = {"GB/s": round(wbytes / (ms / 1e3) / 1e9, 1),
-                                           "ms": round(ms, 5)}
-    for v in res.values():
-        if isinstance(v, dict) and "GB/s" in v:
-            v["frac"] = round(v["GB/s"] / peak, 3)
+    # 16x16 weight quantize 14336 x 4096 bf16 (and fp32)
+    for dt in (torch.bfloat16, torch.float32):
+        w = workloads.weight(14336, 4096, seed=0, dtype=dt, device=dev)
+        wa = fos.amax(w)
+        c = fos.Config(block16x16=True)
+        wc = torch.empty(14336, 2048, dtype=torch.uint8, device=dev)
+        wsc = torch.empty(896, 256, dtype=torch.uint8, device=dev)
+        ms = _graph_ms(lambda: fos.quantize(w, c, amax=wa, codes=wc, scales=wsc), 4, stream)
+        esz = 2 if dt == torch.bfloat16 else 4
+        rec("weight_16x16_14336x4096_" + ("bf16" if esz == 2 else "fp32"),
+            14336 * 4096 * (esz + 0.5 + 1 / 256), ms)
+        del w
     return res
 
 

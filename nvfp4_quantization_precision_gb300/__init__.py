@@ -128,13 +128,15 @@ def scales_shape(rows, cols, block16x16):
     return (rows // 16 if block16x16 else rows, cols // 16)
 
 
-def quantize(x, cfg=Config(), amax=None, codes=None, scales=None):
-    """Quantize x [rows, cols] (bf16 / fp16 / fp32).  With amax=None the
-    library computes the amax (per tensor or per row) and returns it."""
+def quantize(x, cfg=Config(), amax=None, codes=None, scales=None, amax_given=None):
+    """Quantize x [rows, cols] (bf16 / fp16 / fp32).  amax is read when
+    given (the default when a tensor is passed); with amax_given=False it is
+    an output buffer the library fills.  With amax=None it is allocated,
+    computed and returned."""
     _cuda(x, "x")
     R, C = x.shape
     dev = x.device
-    given = amax is not None
+    given = (amax is not None) if amax_given is None else bool(amax_given)
     if amax is None:
         amax = torch.empty(R if cfg.row_scaled else 1, dtype=torch.float32, device=dev)
     if codes is None:
@@ -159,17 +161,18 @@ def dequantize(codes, scales, amax, cfg=Config(), out_dtype=torch.bfloat16, out=
     return out
 
 
-def qdq(xs, cfg=Config(), amaxes=None, outs=None):
+def qdq(xs, cfg=Config(), amaxes=None, outs=None, amax_given=None):
     """Fused quantize-dequantize of a list of rank-2 bf16/fp16 tensors in one
-    launch.  amaxes: list of 1-element float32 tensors (given) or None (the
-    library computes them).  Returns the list of outputs."""
+    launch.  amaxes: list of 1-element float32 tensors, read when given (the
+    default when passed) or filled when amax_given=False; None allocates and
+    computes them.  Returns the list of outputs."""
     n = len(xs)
     if n == 0:
         return []
     for x in xs:
         _cuda(x, "x")
     dt = xs[0].dtype
-    given = amaxes is not None
+    given = (amaxes is not None) if amax_given is None else bool(amax_given)
     if amaxes is None:
         amaxes = [torch.empty(1, dtype=torch.float32, device=x.device) for x in xs]
     if outs is None:
@@ -186,7 +189,8 @@ def qdq(xs, cfg=Config(), amaxes=None, outs=None):
     return outs
 
 
-def quantize_grouped(x, offs, cfg=Config(), group_amax=None, codes=None, scales=None):
+def quantize_grouped(x, offs, cfg=Config(), group_amax=None, codes=None, scales=None,
+                     amax_given=None):
     """One call over a packed token tensor split into groups by cumulative
     ends offs (int32, device).  Rows past offs[-1] get zero codes/scales."""
     _cuda(x, "x")
@@ -196,7 +200,7 @@ def quantize_grouped(x, offs, cfg=Config(), group_amax=None, codes=None, scales=
     R, C = x.shape
     G = offs.numel()
     dev = x.device
-    given = group_amax is not None
+    given = (group_amax is not None) if amax_given is None else bool(amax_given)
     if group_amax is None:
         group_amax = torch.empty(G, dtype=torch.float32, device=dev)
     if codes is None:

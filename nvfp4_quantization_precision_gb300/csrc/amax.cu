@@ -7,7 +7,7 @@ template <In IT>
 static cudaError_t by_scope(Src scope, const AmaxArgs& a, cudaStream_t s) {
     switch (scope) {
         case Src::TENSOR:
-            return launch_persistent(k_amax_tensor<IT>, a, a.units, ring_smem_bytes<IT>(), s);
+            return launch_persistent(k_amax_tensor<IT>, a, a.units, 0, s);
         case Src::ROW:
             return launch_persistent(k_amax_rows<IT>, a, (a.rows + 0), 0, s);
         case Src::GROUP:

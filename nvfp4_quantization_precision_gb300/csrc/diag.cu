@@ -51,7 +51,7 @@ __global__ void k_diag(int op, const void* in, void* out, int64_t n) {
                 }
                 break;
             case FOS_DIAG_DIV6:
-                static_cast<float*>(out)[i] = fdiv(fi[i], 6.0f);
+                static_cast<float*>(out)[i] = div6_rn(fi[i]);
                 break;
             default:
                 break;

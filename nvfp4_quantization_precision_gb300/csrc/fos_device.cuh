@@ -88,6 +88,41 @@ __device__ __forceinline__ uint32_t e2m1x2(uint64_t y) {
         : "=r"(r) : "l"(y));
     return r;
 }
+// Encode a pair to E2M1 and decode the result in one step: `byte` receives
+// the packed codes (low nibble = low element), `h` their exact values as
+// f16x2 (low half = low element).
+__device__ __forceinline__ void e2m1x2_enc_dec(uint64_t y, uint32_t& byte, uint32_t& h) {
+    asm("{\n\t.reg .b8 q;\n\t.reg .f32 lo, hi;\n\tmov.b64 {lo, hi}, %2;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 q, hi, lo;\n\tcvt.rn.f16x2.e2m1x2 %1, q;\n\t"
+        "cvt.u32.u8 %0, q;\n\t}"
+        : "=r"(byte), "=r"(h) : "l"(y));
+}
+// Four pairs at once: encode y[0..3] to E2M1, return the four code bytes
+// packed into one word (byte k = pair k, low nibble = low element) and, with
+// DEC, the exact decodes as f16x2 (h[k] low half = low element of pair k).
+template <bool DEC>
+__device__ __forceinline__ void e2m1x8(const uint64_t* y, uint32_t& word, uint32_t* h) {
+    if constexpr (DEC) {
+        asm("{\n\t.reg .b8 q0, q1, q2, q3;\n\t.reg .f32 a0, b0, a1, b1, a2, b2, a3, b3;\n\t"
+            "mov.b64 {a0, b0}, %5;\n\tmov.b64 {a1, b1}, %6;\n\t"
+            "mov.b64 {a2, b2}, %7;\n\tmov.b64 {a3, b3}, %8;\n\t"
+            "cvt.rn.satfinite.e2m1x2.f32 q0, b0, a0;\n\tcvt.rn.satfinite.e2m1x2.f32 q1, b1, a1;\n\t"
+            "cvt.rn.satfinite.e2m1x2.f32 q2, b2, a2;\n\tcvt.rn.satfinite.e2m1x2.f32 q3, b3, a3;\n\t"
+            "cvt.rn.f16x2.e2m1x2 %1, q0;\n\tcvt.rn.f16x2.e2m1x2 %2, q1;\n\t"
+            "cvt.rn.f16x2.e2m1x2 %3, q2;\n\tcvt.rn.f16x2.e2m1x2 %4, q3;\n\t"
+            "mov.b32 %0, {q0, q1, q2, q3};\n\t}"
+            : "=r"(word), "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+            : "l"(y[0]), "l"(y[1]), "l"(y[2]), "l"(y[3]));
+    } else {
+        asm("{\n\t.reg .b8 q0, q1, q2, q3;\n\t.reg .f32 a0, b0, a1, b1, a2, b2, a3, b3;\n\t"
+            "mov.b64 {a0, b0}, %1;\n\tmov.b64 {a1, b1}, %2;\n\t"
+            "mov.b64 {a2, b2}, %3;\n\tmov.b64 {a3, b3}, %4;\n\t"
+            "cvt.rn.satfinite.e2m1x2.f32 q0, b0, a0;\n\tcvt.rn.satfinite.e2m1x2.f32 q1, b1, a1;\n\t"
+            "cvt.rn.satfinite.e2m1x2.f32 q2, b2, a2;\n\tcvt.rn.satfinite.e2m1x2.f32 q3, b3, a3;\n\t"
+            "mov.b32 %0, {q0, q1, q2, q3};\n\t}"
+            : "=r"(word) : "l"(y[0]), "l"(y[1]), "l"(y[2]), "l"(y[3]));
+    }
+}
 // Exact decode of an E2M1 pair byte to f16x2 (low half = low nibble).
 __device__ __forceinline__ uint32_t e2m1x2_f16x2(uint32_t byte) {
     uint32_t r;
@@ -132,6 +167,17 @@ __device__ __forceinline__ float e4m3_f32(uint32_t code) {
     return f;
 }
 
+// ------------------------------------------------------------ launch chaining
+// Programmatic dependent launch: kernels are launched so that the next kernel
+// in the stream may be placed on the SMs while this one drains.  Every kernel
+// waits for the previous grid (completion and memory visibility) before its
+// first global read, then lets its own dependents launch.  On a launch
+// without the attribute both instructions have no effect.
+__device__ __forceinline__ void chain_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void chain_release() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------ memory
 __device__ __forceinline__ void ld256(const void* p, uint32_t* w) {
     asm volatile("ld.global.nc.L1::no_allocate.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
@@ -150,63 +196,6 @@ __device__ __forceinline__ void st64(void* p, uint32_t a, uint32_t b) {
 __device__ __forceinline__ void st8(void* p, uint32_t a) {
     asm volatile("st.global.u8 [%0], %1;" ::"l"(p), "r"(a) : "memory");
 }
-
-// ------------------------------------------------------------ per-lane ring
-// Input staging through shared memory with cp.async: every lane copies its
-// own 16-element segment (32 B, or 64 B for fp32) into a ring of kDepth
-// stages and later reads back only what it copied itself, so no cross-lane
-// synchronisation is needed; cp.async.wait_group is a hardware wait on the
-// lane's own copies.  Keeping kDepth - 1 segments in flight per lane holds
-// enough bytes in flight per SM to cover HBM latency without spending
-// registers on prefetch buffers.  Within a stage the two (or four) 16-byte
-// quarters of the lanes are laid out quarter-major so that each 128-bit
-// shared load of a warp is conflict-free.
-constexpr int kDepth = 4;
-
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
-    // src-size 0 writes 16 zero bytes and reads nothing from global memory
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
-                 "r"(valid ? 16 : 0)
-                 : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() {
-    asm volatile("cp.async.commit_group;" ::: "memory");
-}
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-__device__ __forceinline__ void lds128(uint32_t addr, uint32_t* w) {
-    asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
-                 : "r"(addr));
-}
-
-template <int kQuarters>  // 16-byte pieces per lane segment: 2 (16-bit input) or 4 (fp32)
-struct LaneRing {
-    static constexpr int kStageBytes = kQuarters * 32 * 16;  // per warp
-    static constexpr int kBytes = kStageBytes * kDepth;
-    uint32_t base;  // shared address of this warp's ring
-    int lane;
-    __device__ __forceinline__ LaneRing(void* smem_warp, int l)
-        : base((uint32_t)__cvta_generic_to_shared(smem_warp)), lane(l) {}
-    __device__ __forceinline__ uint32_t at(int stage, int q) const {
-        return base + stage * kStageBytes + q * 512 + lane * 16;
-    }
-    // Copies the lane's segment into `stage` -- or zeros when !valid, in which
-    // case nothing is read and `src` only has to be a mapped address -- and
-    // closes the commit group.
-    __device__ __forceinline__ void issue(int stage, const void* src, bool valid) {
-        const char* p = static_cast<const char*>(src);
-#pragma unroll
-        for (int q = 0; q < kQuarters; ++q) cp_async16(at(stage, q), p + (valid ? 16 * q : 0), valid);
-        cp_async_commit();
-    }
-    __device__ __forceinline__ void read(int stage, uint32_t* w) const {
-#pragma unroll
-        for (int q = 0; q < kQuarters; ++q) lds128(at(stage, q), w + 4 * q);
-    }
-};
 
 // Raw storage of one 16-element row segment.
 template <In IT>
@@ -243,13 +232,18 @@ __device__ __forceinline__ void widen(const Raw<IT>& r, uint64_t (&xp)[8]) {
 
 // NaN-dropping max|x| over the 16 elements, initial +0 (max.f32 returns the
 // non-NaN operand; the final max with +0 maps an all-NaN segment to 0).
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
 __device__ __forceinline__ float seg_amax(const uint64_t (&xp)[8]) {
     float m = 0.0f;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
         float a, b;
         upk(xp[j], a, b);
-        m = fmaxf(m, fmaxf(fabsf(a), fabsf(b)));
+        m = max3(m, fabsf(a), fabsf(b));
     }
     return m;
 }
@@ -294,43 +288,80 @@ __device__ __forceinline__ uint32_t out_pair(uint64_t v) {
     else return f32x2_f16x2(v);
 }
 
+// e = h - x for an f16 pair h (widened exactly) and an f32 pair x: the
+// negated FP16-mode error, which has the same magnitude and square.
+__device__ __forceinline__ uint64_t sub2_f16(uint32_t h, uint64_t x) {
+    float xl, xh, el, eh;
+    upk(x, xl, xh);
+    asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
+        "sub.rn.f32.f16 %0, a, %3;\n\tsub.rn.f32.f16 %1, b, %4;\n\t}"
+        : "=f"(el), "=f"(eh) : "r"(h), "f"(xl), "f"(xh));
+    return pk(el, eh);
+}
+
 // One candidate of one 16-element row segment under common scales (r, d).
-// Encodes y = x * r to E2M1, decodes exactly, and returns the segment's
-// error reduced by the pinned tree (for w = 8,4,2,1: t[i] += t[i+w], i < w);
-// element pairs (2j, 2j+1) sit in one packed register, so the first three
-// tree levels are packed adds of pairs (j, j+4), (j, j+2), (0, 1).
+// Encodes y = x * r to E2M1, decodes exactly, and returns the
+// segment's error reduced by the pinned tree (for w = 8,4,2,1: t[i] +=
+// t[i+w], i < w).  Element pairs (2j, 2j+1) sit in one packed register, so
+// tree levels are packed adds of pairs (j, j+4), (j, j+2), (0, 1); for MAE
+// the first level is done on scalars so that |e| folds into the add.
 // With OT != NONE it also returns the decode v * d rounded to the output type.
 template <Err EM, Out OT>
 __device__ __forceinline__ float candidate(const uint64_t (&xp)[8], float r, float d,
                                            uint64_t nz, uint32_t (&code)[2],
                                            uint32_t (&out)[8]) {
     const uint64_t rr = pk(r, r), dd = pk(d, d);
-    uint32_t q[8];
+    constexpr bool kDec = (EM != Err::STD) || (OT != Out::NONE);
     uint64_t term[8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        q[j] = e2m1x2(mul2(xp[j], rr));
-        if constexpr (EM != Err::STD) {
-            uint64_t deq = mul2_nc(f16x2_f32x2(e2m1x2_f16x2(q[j])), dd, nz);
-            if constexpr (OT != Out::NONE) out[j] = out_pair<OT>(deq);
-            if constexpr (err_is_f16(EM)) {
-                const uint32_t h = (OT == Out::F16) ? out[j] : f32x2_f16x2(deq);
-                deq = f16x2_f32x2(h);
+    for (int g = 0; g < 2; ++g) {
+        uint64_t y[4];
+        uint32_t h[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) y[k] = mul2(xp[4 * g + k], rr);
+        e2m1x8<kDec>(y, code[g], h);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int j = 4 * g + k;
+            if constexpr (EM != Err::STD) {
+                const uint64_t deq = mul2_nc(f16x2_f32x2(h[k]), dd, nz);
+                if constexpr (OT != Out::NONE) out[j] = out_pair<OT>(deq);
+                uint64_t e;
+                if constexpr (err_is_f16(EM)) {
+                    e = sub2_f16((OT == Out::F16) ? out[j] : f32x2_f16x2(deq), xp[j]);
+                } else {
+                    e = sub2(xp[j], deq);
+                }
+                term[j] = err_is_mse(EM) ? mul2_nc(e, e, nz) : e;
+            } else if constexpr (OT != Out::NONE) {
+                out[j] = out_pair<OT>(mul2(f16x2_f32x2(h[k]), dd));
             }
-            const uint64_t e = sub2(xp[j], deq);
-            term[j] = err_is_mse(EM) ? mul2_nc(e, e, nz) : abs2(e);
-        } else {
-            if constexpr (OT != Out::NONE)
-                out[j] = out_pair<OT>(mul2(f16x2_f32x2(e2m1x2_f16x2(q[j])), dd));
         }
     }
-    code[0] = pack4(q[0], q[1], q[2], q[3]);
-    code[1] = pack4(q[4], q[5], q[6], q[7]);
     if constexpr (EM == Err::STD) {
         return 0.0f;
     } else {
-        const uint64_t t0 = add2(term[0], term[4]), t1 = add2(term[1], term[5]);
-        const uint64_t t2 = add2(term[2], term[6]), t3 = add2(term[3], term[7]);
+        uint64_t t0, t1, t2, t3;
+        if constexpr (err_is_mse(EM)) {
+            t0 = add2(term[0], term[4]);
+            t1 = add2(term[1], term[5]);
+            t2 = add2(term[2], term[6]);
+            t3 = add2(term[3], term[7]);
+        } else {
+            float s[8];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                float al, ah, bl, bh;
+                upk(term[j], al, ah);
+                upk(term[j + 4], bl, bh);
+                s[2 * j] = fadd(fabsf(al), fabsf(bl));
+                s[2 * j + 1] = fadd(fabsf(ah), fabsf(bh));
+            }
+            t0 = pk(s[0], s[1]);
+            t1 = pk(s[2], s[3]);
+            t2 = pk(s[4], s[5]);
+            t3 = pk(s[6], s[7]);
+        }
         const uint64_t u0 = add2(t0, t2), u1 = add2(t1, t3);
         float a, b;
         upk(add2(u0, u1), a, b);
@@ -338,12 +369,29 @@ __device__ __forceinline__ float candidate(const uint64_t (&xp)[8], float r, flo
     }
 }
 
+// Correctly rounded t / 6 for t >= 0.  In the range where the quotient is a
+// normal number the division by the constant uses Markstein's correction:
+// with c = rn(1/6), q = rn(t * c) is within an ulp of t / 6, the remainder
+// r = t - 6q is exact in one fma, and rn(q + r * c) is the correctly rounded
+// quotient (P. Markstein, "IA-64 and Elementary Functions", 2000, division
+// by a correctly rounded reciprocal).  Subnormal quotients, Inf and NaN take
+// the full division.  Checked against IEEE division for all 2^32 inputs.
+__device__ __forceinline__ float div6_rn(float t) {
+    constexpr float kInv6 = 0x1.555556p-3f;  // rn(1/6), bits 0x3E2AAAAB
+    if (t >= 0x1.8p-124f && t <= kFltMax) {  // 6 * 2^-126 .. FLT_MAX
+        const float q = fmul(t, kInv6);
+        const float r = __fmaf_rn(-q, 6.0f, t);
+        return __fmaf_rn(r, kInv6, q);
+    }
+    return fdiv(t, 6.0f);
+}
+
 // Block-scale codes of the two candidates for a block (tile) amax:
 // s_k = (amax * S) / k, E4M3 RN satfinite.  Low byte: map-to-6, high byte:
 // map-to-4 (t / 4 is the exact product t * 0.25).
 __device__ __forceinline__ uint32_t scale_codes(float amax, float S) {
     const float t = fmul(amax, S);
-    return e4m3x2(fdiv(t, 6.0f), fmul(t, 0.25f));
+    return e4m3x2(div6_rn(t), fmul(t, 0.25f));
 }
 
 // Full 1x16 block: returns codes (2 words), the E4M3 scale byte, and with

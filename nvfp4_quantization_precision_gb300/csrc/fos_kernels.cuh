@@ -71,17 +71,7 @@ struct AmaxArgs {
     int64_t rows, nb, units;
 };
 
-template <In IT>
-using RingOf = LaneRing<(IT == In::F32) ? 4 : 2>;
-
-// Shared memory of the encode kernels: the per-warp input rings, then (GROUP)
-// the clamped group ends.
-template <In IT>
-__host__ __device__ constexpr size_t ring_smem_bytes() {
-    return (size_t)kWarps * RingOf<IT>::kBytes;
-}
-
-// Position of a (row, 32-block chunk) walk.
+// Position of a (row, chunk) walk.
 struct RowChunk {
     int64_t row, chunk;
     __device__ __forceinline__ void next(int64_t cpr) {
@@ -89,211 +79,196 @@ struct RowChunk {
     }
 };
 
+template <In IT>
+__device__ __forceinline__ void load_if(Raw<IT>& r, const char* p, bool v) {
+    if (v) load_seg<IT>(r, p);
+}
+
 // ------------------------------------------------------------------------
-// 1x16 quantize (codes + scales).
+// 1x16 quantize with a per-tensor scale.  Grid-stride over 32-block units:
+// in each step the grid sweeps one contiguous window of the tensor; every
+// lane loads its next block one step ahead.
+// ------------------------------------------------------------------------
+template <In IT, Err EM>
+__global__ void __launch_bounds__(kThreads) k_quant1x16_tensor(const EncArgs a) {
+    chain_wait();
+    chain_release();
+    __shared__ float2 s_tbl[kWarps][128];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    float2* tbl = s_tbl[warp];
+    const uint64_t nz = pk(a.neg_zero, a.neg_zero);
+    const int64_t nw = (int64_t)gridDim.x * kWarps;
+    const int64_t u = (int64_t)blockIdx.x * kWarps + warp;
+    if (u >= a.units) return;
+    constexpr int64_t kBytes = (IT == In::F32) ? 64 : 32;
+    const char* xb = static_cast<const char*>(a.x);
+    // Two units per iteration with two register buffers (A: u, B: u + nw):
+    // each buffer is refilled one step ahead without register copies.
+    const int64_t step = nw * 32;
+    int64_t b = u * 32 + lane;
+    Raw<IT> ra, rb;
+    load_if<IT>(ra, xb + b * kBytes, b < a.nblk);
+    const float S = global_scale(a.amax[0], a.six_bound);
+    build_table(tbl, S, lane);
+    uint32_t dummy[8];
+    auto encode = [&](const Raw<IT>& r, int64_t blk) {
+        uint64_t xp[8];
+        widen<IT>(r, xp);
+        uint32_t code[2], scale;
+        encode_block<EM, Out::NONE>(xp, S, tbl, nz, code, scale, dummy);
+        st64(a.codes + blk * 8, code[0], code[1]);
+        st8(a.scales + blk, scale);
+    };
+    for (; b < a.nblk + lane; b += 2 * step) {  // b - lane is the first block of the unit
+        load_if<IT>(rb, xb + (b + step) * kBytes, b + step < a.nblk);
+        if (b < a.nblk) encode(ra, b);
+        load_if<IT>(ra, xb + (b + 2 * step) * kBytes, b + 2 * step < a.nblk);
+        if (b + step < a.nblk) encode(rb, b + step);
+    }
+}
+
+// ------------------------------------------------------------------------
+// 1x16 quantize with a per-row or per-group scale.  Each warp walks one
+// contiguous range of (row, 32-block chunk) units so that the global scale
+// (and its table) changes only at row / group boundaries.
 // ------------------------------------------------------------------------
 template <In IT, Err EM, Src SRC>
 __global__ void __launch_bounds__(kThreads) k_quant1x16(const EncArgs a) {
-    extern __shared__ __align__(16) unsigned char s_dyn[];
+    chain_wait();
+    chain_release();
+    extern __shared__ int32_t s_ends[];
     __shared__ float2 s_tbl[kWarps][128];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    int32_t* s_ends = reinterpret_cast<int32_t*>(s_dyn + ring_smem_bytes<IT>());
     if constexpr (SRC == Src::GROUP) load_group_ends(s_ends, a.offs, a.G, a.rows);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     float2* tbl = s_tbl[warp];
-    RingOf<IT> ring(s_dyn + warp * RingOf<IT>::kBytes, lane);
     const uint64_t nz = pk(a.neg_zero, a.neg_zero);
     const int64_t nw = (int64_t)gridDim.x * kWarps, gw = (int64_t)blockIdx.x * kWarps + warp;
     const int64_t u0 = split_at(a.units, nw, gw), u1 = split_at(a.units, nw, gw + 1);
     if (u0 >= u1) return;
     constexpr int64_t kBytes = (IT == In::F32) ? 64 : 32;
     const char* xb = static_cast<const char*>(a.x);
+    int64_t last_end = a.rows;
+    if constexpr (SRC == Src::GROUP) last_end = s_ends[a.G - 1];
+    RowChunk cc{u0 / a.cpr, u0 % a.cpr};
+    int64_t j = cc.chunk * 32 + lane;
+    Raw<IT> cur;
+    load_if<IT>(cur, xb + (cc.row * a.nb + j) * kBytes, j < a.nb && cc.row < last_end);
+    int g = 0;
+    if constexpr (SRC == Src::GROUP)
+        while (g < a.G && cc.row >= s_ends[g]) ++g;
+    int64_t key = -1;
+    float S = 1.0f;
     uint32_t dummy[8];
-
-    if constexpr (SRC == Src::TENSOR) {
-        // issue the first kDepth-1 units before anything else
-#pragma unroll
-        for (int s = 0; s < kDepth - 1; ++s) {
-            const int64_t b = (u0 + s) * 32 + lane;
-            const bool v = (u0 + s < u1) && b < a.nblk;
-            ring.issue(s, xb + (v ? b : 0) * kBytes, v);
+    for (int64_t u = u0; u < u1; ++u) {
+        RowChunk nc = cc;
+        nc.next(a.cpr);
+        const int64_t jn = nc.chunk * 32 + lane;
+        Raw<IT> nxt;
+        load_if<IT>(nxt, xb + (nc.row * a.nb + jn) * kBytes,
+                    u + 1 < u1 && jn < a.nb && nc.row < last_end);
+        int64_t k;
+        if constexpr (SRC == Src::ROW) {
+            k = cc.row;
+        } else {
+            while (g < a.G && cc.row >= s_ends[g]) ++g;
+            k = g;  // g == G: tail past the last group end
         }
-        const float S = global_scale(a.amax[0], a.six_bound);
-        build_table(tbl, S, lane);
-        int stage = 0;
-        for (int64_t u = u0; u < u1; ++u) {
-            const int64_t ui = u + kDepth - 1, bi = ui * 32 + lane;
-            const bool vi = ui < u1 && bi < a.nblk;
-            ring.issue((stage + kDepth - 1) % kDepth, xb + (vi ? bi : 0) * kBytes, vi);
-            cp_async_wait<kDepth - 1>();
-            const int64_t b = u * 32 + lane;
-            if (b < a.nblk) {
-                Raw<IT> cur;
-                ring.read(stage, cur.w);
+        if (k != key) {
+            key = k;
+            if (SRC == Src::ROW || k < a.G) {
+                S = global_scale(a.amax[k], a.six_bound);
+                build_table(tbl, S, lane);
+            }
+        }
+        const int64_t b = cc.row * a.nb + j;
+        if (j < a.nb) {
+            if (cc.row < last_end) {
                 uint64_t xp[8];
                 widen<IT>(cur, xp);
                 uint32_t code[2], scale;
                 encode_block<EM, Out::NONE>(xp, S, tbl, nz, code, scale, dummy);
                 st64(a.codes + b * 8, code[0], code[1]);
                 st8(a.scales + b, scale);
+            } else {  // zero-extended tail of a padded grouped tensor
+                st64(a.codes + b * 8, 0u, 0u);
+                st8(a.scales + b, 0u);
             }
-            stage = (stage + 1) % kDepth;
         }
-    } else {
-        // (row, chunk) walk; the key is the row (ROW) or its group (GROUP).
-        int64_t last_end = a.rows;
-        if constexpr (SRC == Src::GROUP) last_end = s_ends[a.G - 1];
-        RowChunk cc{u0 / a.cpr, u0 % a.cpr}, ic = cc;
-#pragma unroll
-        for (int s = 0; s < kDepth - 1; ++s) {
-            const int64_t j = ic.chunk * 32 + lane;
-            const bool v = (u0 + s < u1) && j < a.nb && ic.row < last_end;
-            ring.issue(s, xb + (v ? ic.row * a.nb + j : 0) * kBytes, v);
-            ic.next(a.cpr);
-        }
-        int g = 0;
-        if constexpr (SRC == Src::GROUP)
-            while (g < a.G && cc.row >= s_ends[g]) ++g;
-        int64_t key = -1;
-        float S = 1.0f;
-        int stage = 0;
-        for (int64_t u = u0; u < u1; ++u) {
-            {
-                const int64_t j = ic.chunk * 32 + lane;
-                const bool v = (u + kDepth - 1 < u1) && j < a.nb && ic.row < last_end;
-                ring.issue((stage + kDepth - 1) % kDepth, xb + (v ? ic.row * a.nb + j : 0) * kBytes,
-                           v);
-                ic.next(a.cpr);
-            }
-            // global scale of this unit
-            int64_t k;
-            if constexpr (SRC == Src::ROW) {
-                k = cc.row;
-            } else {
-                while (g < a.G && cc.row >= s_ends[g]) ++g;
-                k = g;  // g == G: tail past the last group end
-            }
-            if (k != key) {
-                key = k;
-                if (SRC == Src::ROW || k < a.G) {
-                    S = global_scale(a.amax[k], a.six_bound);
-                    build_table(tbl, S, lane);
-                }
-            }
-            cp_async_wait<kDepth - 1>();
-            const int64_t j = cc.chunk * 32 + lane;
-            const int64_t b = cc.row * a.nb + j;
-            if (j < a.nb) {
-                if (cc.row < last_end) {
-                    Raw<IT> cur;
-                    ring.read(stage, cur.w);
-                    uint64_t xp[8];
-                    widen<IT>(cur, xp);
-                    uint32_t code[2], scale;
-                    encode_block<EM, Out::NONE>(xp, S, tbl, nz, code, scale, dummy);
-                    st64(a.codes + b * 8, code[0], code[1]);
-                    st8(a.scales + b, scale);
-                } else {  // zero-extended tail of a padded grouped tensor
-                    st64(a.codes + b * 8, 0u, 0u);
-                    st8(a.scales + b, 0u);
-                }
-            }
-            cc.next(a.cpr);
-            stage = (stage + 1) % kDepth;
-        }
+        cur = nxt;
+        cc = nc;
+        j = jn;
     }
-    cp_async_wait<0>();
 }
 
 // ------------------------------------------------------------------------
 // Fused quantize-dequantize over a list of tensors (per-tensor scale, 1x16),
 // output dtype == input dtype (bf16 / fp16).  Codes and scales never leave
-// registers.  Units are 32-block chunks of one tensor; empty tensors own no
-// units.
+// registers.  Grid-stride over the concatenated 32-block units of the list
+// (empty tensors own no units); the per-warp table is rebuilt whenever the
+// warp's unit moves into the next tensor.
 // ------------------------------------------------------------------------
-struct ListPos {
-    int t;
-    int64_t u;  // global unit index
-};
-
 template <In IT, Err EM>
 __global__ void __launch_bounds__(kThreads) k_qdq1x16(const __grid_constant__ QdqArgs a) {
+    chain_wait();
+    chain_release();
     static_assert(IT != In::F32, "fused QDQ is bf16 / fp16 only");
     constexpr Out OT = (IT == In::BF16) ? Out::BF16 : Out::F16;
-    extern __shared__ __align__(16) unsigned char s_dyn[];
     __shared__ float2 s_tbl[kWarps][128];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     float2* tbl = s_tbl[warp];
-    RingOf<IT> ring(s_dyn + warp * RingOf<IT>::kBytes, lane);
     const uint64_t nz = pk(a.neg_zero, a.neg_zero);
-    const int64_t nw = (int64_t)gridDim.x * kWarps, gw = (int64_t)blockIdx.x * kWarps + warp;
-    const int64_t u0 = split_at(a.units, nw, gw), u1 = split_at(a.units, nw, gw + 1);
-    if (u0 >= u1) return;
-    // tensor of a unit: advance while the next tensor starts at or before it
-    auto seek = [&](ListPos& p) {
-        while (p.t < a.n && a.t[p.t + 1].unit_begin <= p.u) ++p.t;
-    };
-    ListPos cp{0, u0};
-    seek(cp);
-    ListPos ip = cp;
-#pragma unroll
-    for (int s = 0; s < kDepth - 1; ++s) {
-        const QdqTensor& T = a.t[ip.t];
-        const int64_t b = (ip.u - T.unit_begin) * 32 + lane;
-        const bool v = ip.u < u1 && b < T.nblk;
-        ring.issue(s, static_cast<const char*>(v ? T.x : a.t[cp.t].x) + (v ? b : 0) * 32, v);
-        ++ip.u;
-        seek(ip);
-    }
+    const int64_t nw = (int64_t)gridDim.x * kWarps;
+    int64_t u = (int64_t)blockIdx.x * kWarps + warp;
+    if (u >= a.units) return;
+    int t = 0;
+    while (t < a.n && a.t[t + 1].unit_begin <= u) ++t;
+    int64_t b = (u - a.t[t].unit_begin) * 32 + lane;
+    bool v = b < a.t[t].nblk;
+    Raw<IT> cur;
+    load_if<IT>(cur, static_cast<const char*>(a.t[t].x) + b * 32, v);
     int ti = -1;
     float S = 1.0f;
-    int stage = 0;
-    for (int64_t u = u0; u < u1; ++u) {
-        {
-            const QdqTensor& T = a.t[ip.t];
-            const int64_t b = (ip.u - T.unit_begin) * 32 + lane;
-            const bool v = ip.u < u1 && b < T.nblk;
-            ring.issue((stage + kDepth - 1) % kDepth,
-                       static_cast<const char*>(v ? T.x : a.t[cp.t].x) + (v ? b : 0) * 32, v);
-            ++ip.u;
-            seek(ip);
-        }
-        if (cp.t != ti) {
-            ti = cp.t;
-            S = global_scale(*a.t[ti].amax, a.six_bound);
+    for (; u < a.units; u += nw) {
+        const int64_t un = u + nw;
+        int tn = t;
+        while (tn < a.n && a.t[tn + 1].unit_begin <= un) ++tn;  // t[n] is a sentinel
+        const int64_t bn = (un - a.t[tn].unit_begin) * 32 + lane;
+        const bool vn = un < a.units && bn < a.t[tn].nblk;
+        Raw<IT> nxt;
+        load_if<IT>(nxt, static_cast<const char*>(a.t[tn].x) + bn * 32, vn);
+        if (t != ti) {
+            ti = t;
+            S = global_scale(*a.t[t].amax, a.six_bound);
             build_table(tbl, S, lane);
         }
-        cp_async_wait<kDepth - 1>();
-        const QdqTensor& T = a.t[cp.t];
-        const int64_t b = (cp.u - T.unit_begin) * 32 + lane;
-        if (b < T.nblk) {
-            Raw<IT> cur;
-            ring.read(stage, cur.w);
+        if (v) {
             uint64_t xp[8];
             widen<IT>(cur, xp);
             uint32_t code[2], scale, out[8];
             encode_block<EM, OT>(xp, S, tbl, nz, code, scale, out);
-            st256(static_cast<char*>(T.out) + b * 32, out);
+            st256(static_cast<char*>(a.t[t].out) + b * 32, out);
         }
-        ++cp.u;
-        seek(cp);
-        stage = (stage + 1) % kDepth;
+        cur = nxt;
+        t = tn;
+        b = bn;
+        v = vn;
     }
-    cp_async_wait<0>();
 }
 
 // ------------------------------------------------------------------------
 // 16x16 quantize.  Unit = (band of 16 rows, pair of 16x16 tiles); lane l
-// holds row (l & 15) of tile (2 * pair + (l >> 4)).
+// holds row (l & 15) of tile (2 * pair + (l >> 4)).  Contiguous unit range
+// per warp, next unit loaded one step ahead.
 // ------------------------------------------------------------------------
 template <In IT, Err EM, Src SRC>
 __global__ void __launch_bounds__(kThreads) k_quant16x16(const EncArgs a) {
-    extern __shared__ __align__(16) unsigned char s_dyn[];
+    chain_wait();
+    chain_release();
+    extern __shared__ int32_t s_ends[];
     __shared__ float2 s_tbl[kWarps][128];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    int32_t* s_ends = reinterpret_cast<int32_t*>(s_dyn + ring_smem_bytes<IT>());
     if constexpr (SRC == Src::GROUP) load_group_ends(s_ends, a.offs, a.G, a.rows);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     float2* tbl = s_tbl[warp];
-    RingOf<IT> ring(s_dyn + warp * RingOf<IT>::kBytes, lane);
     const uint64_t nz = pk(a.neg_zero, a.neg_zero);
     const int64_t nw = (int64_t)gridDim.x * kWarps, gw = (int64_t)blockIdx.x * kWarps + warp;
     const int64_t u0 = split_at(a.units, nw, gw), u1 = split_at(a.units, nw, gw + 1);
@@ -304,19 +279,15 @@ __global__ void __launch_bounds__(kThreads) k_quant16x16(const EncArgs a) {
     const int64_t cols = a.nb * 16;
     int64_t last_end = a.rows;
     if constexpr (SRC == Src::GROUP) last_end = s_ends[a.G - 1];
-    RowChunk cc{u0 / a.cpr, u0 % a.cpr}, ic = cc;  // row = band, chunk = tile pair
-    auto src_of = [&](const RowChunk& p, bool& v) {
+    RowChunk cc{u0 / a.cpr, u0 % a.cpr};  // row = band, chunk = tile pair
+    auto load_unit = [&](Raw<IT>& r, const RowChunk& p, bool in_range) {
         const int64_t J = p.chunk * 2 + half;
-        v = J < a.nb && p.row * 16 < last_end;
-        return xb + (v ? ((p.row * 16 + r16) * cols + J * 16) * kElt : 0);
+        zero_seg<IT>(r);
+        if (in_range && J < a.nb && p.row * 16 < last_end)
+            load_seg<IT>(r, xb + ((p.row * 16 + r16) * cols + J * 16) * kElt);
     };
-#pragma unroll
-    for (int s = 0; s < kDepth - 1; ++s) {
-        bool v;
-        const char* src = src_of(ic, v);
-        ring.issue(s, src, v && (u0 + s < u1));
-        ic.next(a.cpr);
-    }
+    Raw<IT> cur;
+    load_unit(cur, cc, true);
     int g = 0;
     if constexpr (SRC == Src::GROUP)
         while (g < a.G && cc.row * 16 >= s_ends[g]) ++g;
@@ -326,14 +297,11 @@ __global__ void __launch_bounds__(kThreads) k_quant16x16(const EncArgs a) {
         S = global_scale(a.amax[0], a.six_bound);
         build_table(tbl, S, lane);
     }
-    int stage = 0;
     for (int64_t u = u0; u < u1; ++u) {
-        {
-            bool v;
-            const char* src = src_of(ic, v);
-            ring.issue((stage + kDepth - 1) % kDepth, src, v && (u + kDepth - 1 < u1));
-            ic.next(a.cpr);
-        }
+        RowChunk nc = cc;
+        nc.next(a.cpr);
+        Raw<IT> nxt;
+        load_unit(nxt, nc, u + 1 < u1);
         const int64_t band = cc.row;
         bool tail = false;
         if constexpr (SRC != Src::TENSOR) {
@@ -353,14 +321,11 @@ __global__ void __launch_bounds__(kThreads) k_quant16x16(const EncArgs a) {
                 }
             }
         }
-        cp_async_wait<kDepth - 1>();
         const int64_t J = cc.chunk * 2 + half;
         const int64_t row = band * 16 + r16;
         if (!tail) {
-            Raw<IT> cur;
-            ring.read(stage, cur.w);  // zeros for a missing second tile
             uint64_t xp[8];
-            widen<IT>(cur, xp);
+            widen<IT>(cur, xp);  // zeros for a missing second tile
             uint32_t code[2], scale;
             encode_tile_row<EM>(xp, S, tbl, nz, code, scale);  // all lanes take part
             if (J < a.nb) {
@@ -371,10 +336,9 @@ __global__ void __launch_bounds__(kThreads) k_quant16x16(const EncArgs a) {
             st64(a.codes + row * (cols / 2) + J * 8, 0u, 0u);
             if (r16 == 0) st8(a.scales + band * a.nb + J, 0u);
         }
-        cc.next(a.cpr);
-        stage = (stage + 1) % kDepth;
+        cur = nxt;
+        cc = nc;
     }
-    cp_async_wait<0>();
 }
 
 // ------------------------------------------------------------------------
@@ -383,6 +347,8 @@ __global__ void __launch_bounds__(kThreads) k_quant16x16(const EncArgs a) {
 // ------------------------------------------------------------------------
 template <Out OT, bool B16, Src SRC>
 __global__ void __launch_bounds__(kThreads) k_dequant(const DeqArgs a) {
+    chain_wait();
+    chain_release();
     __shared__ float2 s_tbl[kWarps][128];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     float2* tbl = s_tbl[warp];
@@ -447,37 +413,28 @@ __device__ __forceinline__ float warp_max(float m) {
 // non-negative floats like their values.
 template <In IT>
 __global__ void __launch_bounds__(kThreads) k_amax_tensor(const AmaxArgs a) {
-    extern __shared__ __align__(16) unsigned char s_dyn[];
+    chain_wait();
+    chain_release();
     __shared__ float s_m[kWarps];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    RingOf<IT> ring(s_dyn + warp * RingOf<IT>::kBytes, lane);
-    const int64_t nw = (int64_t)gridDim.x * kWarps, gw = (int64_t)blockIdx.x * kWarps + warp;
-    const int64_t u0 = split_at(a.units, nw, gw), u1 = split_at(a.units, nw, gw + 1);
+    const int64_t nw = (int64_t)gridDim.x * kWarps;
     constexpr int64_t kBytes = (IT == In::F32) ? 64 : 32;
     const char* xb = static_cast<const char*>(a.x);
     const int64_t nseg = a.rows * a.nb;
     float m = 0.0f;
-    if (u0 < u1) {
-#pragma unroll
-        for (int s = 0; s < kDepth - 1; ++s) {
-            const int64_t b = (u0 + s) * 32 + lane;
-            const bool v = (u0 + s < u1) && b < nseg;
-            ring.issue(s, xb + (v ? b : 0) * kBytes, v);
-        }
-        int stage = 0;
-        for (int64_t u = u0; u < u1; ++u) {
-            const int64_t ui = u + kDepth - 1, bi = ui * 32 + lane;
-            const bool vi = ui < u1 && bi < nseg;
-            ring.issue((stage + kDepth - 1) % kDepth, xb + (vi ? bi : 0) * kBytes, vi);
-            cp_async_wait<kDepth - 1>();
-            Raw<IT> cur;
-            ring.read(stage, cur.w);  // zeros past the end leave the max unchanged
-            uint64_t xp[8];
-            widen<IT>(cur, xp);
-            m = fmaxf(m, seg_amax(xp));
-            stage = (stage + 1) % kDepth;
-        }
-        cp_async_wait<0>();
+    // grid-stride over 32-segment units, two units in flight per lane
+    for (int64_t u = (int64_t)blockIdx.x * kWarps + warp; u < a.units; u += 2 * nw) {
+        const int64_t s0 = u * 32 + lane, s1 = (u + nw) * 32 + lane;
+        Raw<IT> r0, r1;
+        zero_seg<IT>(r0);
+        zero_seg<IT>(r1);
+        if (s0 < nseg) load_seg<IT>(r0, xb + s0 * kBytes);
+        if (u + nw < a.units && s1 < nseg) load_seg<IT>(r1, xb + s1 * kBytes);
+        uint64_t xp[8];
+        widen<IT>(r0, xp);
+        m = fmaxf(m, seg_amax(xp));
+        widen<IT>(r1, xp);
+        m = fmaxf(m, seg_amax(xp));
     }
     m = warp_max(m);
     if (lane == 0) s_m[warp] = m;
@@ -492,6 +449,8 @@ __global__ void __launch_bounds__(kThreads) k_amax_tensor(const AmaxArgs a) {
 // Per row: one warp per row at a time; amax[r] written directly.
 template <In IT>
 __global__ void __launch_bounds__(kThreads) k_amax_rows(const AmaxArgs a) {
+    chain_wait();
+    chain_release();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t nw = (int64_t)gridDim.x * kWarps, gw = (int64_t)blockIdx.x * kWarps + warp;
     constexpr int64_t kBytes = (IT == In::F32) ? 64 : 32;
@@ -514,6 +473,8 @@ __global__ void __launch_bounds__(kThreads) k_amax_rows(const AmaxArgs a) {
 // folded into amax[g] (cleared by the host) whenever the group changes.
 template <In IT>
 __global__ void __launch_bounds__(kThreads) k_amax_groups(const AmaxArgs a) {
+    chain_wait();
+    chain_release();
     extern __shared__ int32_t s_ends[];
     load_group_ends(s_ends, a.offs, a.G, a.rows);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;

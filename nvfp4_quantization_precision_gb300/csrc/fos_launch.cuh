@@ -26,14 +26,46 @@ inline int sm_count() {
     return cache[dev];
 }
 
+// Resident CTAs per SM of a kernel at a dynamic shared-memory size (cached:
+// the occupancy query costs host time on every launch otherwise).
+inline int resident_ctas(const void* kernel, size_t dyn_smem) {
+    struct Key {
+        const void* k;
+        size_t smem;
+        int dev;
+        bool operator==(const Key& o) const { return k == o.k && smem == o.smem && dev == o.dev; }
+    };
+    struct Hash {
+        size_t operator()(const Key& k) const {
+            return std::hash<const void*>()(k.k) ^ (k.smem * 1315423911u) ^ (size_t)k.dev;
+        }
+    };
+    static std::mutex mu;
+    static std::unordered_map<Key, int, Hash> cache;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const Key key{kernel, dyn_smem, dev};
+    {
+        std::lock_guard<std::mutex> g(mu);
+        auto it = cache.find(key);
+        if (it != cache.end()) return it->second;
+    }
+    int occ = 1;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, kThreads, dyn_smem) !=
+            cudaSuccess || occ < 1) {
+        cudaGetLastError();
+        occ = 1;
+    }
+    std::lock_guard<std::mutex> g(mu);
+    cache[key] = occ;
+    return occ;
+}
+
 // Persistent grid: as many CTAs as stay resident (SMs x occupancy), but no
 // more than one warp per work unit needs.
 template <class Kernel>
 inline int persistent_grid(Kernel kernel, int64_t units, size_t dyn_smem) {
-    int occ = 1;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, kThreads, dyn_smem) !=
-            cudaSuccess || occ < 1)
-        occ = 1;
+    const int occ = resident_ctas(reinterpret_cast<const void*>(kernel), dyn_smem);
     const int64_t full = (int64_t)sm_count() * occ;
     const int64_t need = (units + kWarps - 1) / kWarps;
     int64_t g = need < full ? need : full;
@@ -60,8 +92,18 @@ inline cudaError_t launch_persistent(Kernel kernel, const Args& a, int64_t units
                                      cudaStream_t s) {
     cudaError_t e = allow_smem(reinterpret_cast<const void*>(kernel), dyn_smem);
     if (e != cudaSuccess) return e;
-    const int grid = persistent_grid(kernel, units, dyn_smem);
-    kernel<<<grid, kThreads, dyn_smem, s>>>(a);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)persistent_grid(kernel, units, dyn_smem));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = dyn_smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kernel, a);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

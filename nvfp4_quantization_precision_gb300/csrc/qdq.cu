@@ -6,11 +6,11 @@ namespace fos {
 template <In IT>
 static cudaError_t by_err(Err em, const QdqArgs& a, cudaStream_t s) {
     switch (em) {
-        case Err::STD: return launch_persistent(k_qdq1x16<IT, Err::STD>, a, a.units, ring_smem_bytes<IT>(), s);
-        case Err::MAE: return launch_persistent(k_qdq1x16<IT, Err::MAE>, a, a.units, ring_smem_bytes<IT>(), s);
-        case Err::MSE: return launch_persistent(k_qdq1x16<IT, Err::MSE>, a, a.units, ring_smem_bytes<IT>(), s);
-        case Err::MAE_H: return launch_persistent(k_qdq1x16<IT, Err::MAE_H>, a, a.units, ring_smem_bytes<IT>(), s);
-        case Err::MSE_H: return launch_persistent(k_qdq1x16<IT, Err::MSE_H>, a, a.units, ring_smem_bytes<IT>(), s);
+        case Err::STD: return launch_persistent(k_qdq1x16<IT, Err::STD>, a, a.units, 0, s);
+        case Err::MAE: return launch_persistent(k_qdq1x16<IT, Err::MAE>, a, a.units, 0, s);
+        case Err::MSE: return launch_persistent(k_qdq1x16<IT, Err::MSE>, a, a.units, 0, s);
+        case Err::MAE_H: return launch_persistent(k_qdq1x16<IT, Err::MAE_H>, a, a.units, 0, s);
+        case Err::MSE_H: return launch_persistent(k_qdq1x16<IT, Err::MSE_H>, a, a.units, 0, s);
     }
     return cudaErrorInvalidValue;
 }

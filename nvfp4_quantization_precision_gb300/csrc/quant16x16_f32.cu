@@ -5,8 +5,7 @@ namespace fos {
 
 template <Err EM, Src SRC>
 static cudaError_t go(const EncArgs& a, cudaStream_t s) {
-    const size_t dyn = ring_smem_bytes<In::F32>() +
-                       ((SRC == Src::GROUP) ? sizeof(int32_t) * (size_t)a.G : 0);
+    const size_t dyn = (SRC == Src::GROUP) ? sizeof(int32_t) * (size_t)a.G : 0;
     return launch_persistent(k_quant16x16<In::F32, EM, SRC>, a, a.units, dyn, s);
 }
 

@@ -5,9 +5,12 @@ namespace fos {
 
 template <Err EM, Src SRC>
 static cudaError_t go(const EncArgs& a, cudaStream_t s) {
-    const size_t dyn = ring_smem_bytes<In::BF16>() +
-                       ((SRC == Src::GROUP) ? sizeof(int32_t) * (size_t)a.G : 0);
-    return launch_persistent(k_quant1x16<In::BF16, EM, SRC>, a, a.units, dyn, s);
+    if constexpr (SRC == Src::TENSOR) {
+        return launch_persistent(k_quant1x16_tensor<In::BF16, EM>, a, a.units, 0, s);
+    } else {
+        const size_t dyn = (SRC == Src::GROUP) ? sizeof(int32_t) * (size_t)a.G : 0;
+        return launch_persistent(k_quant1x16<In::BF16, EM, SRC>, a, a.units, dyn, s);
+    }
 }
 
 template <Err EM>

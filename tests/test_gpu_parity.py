@@ -382,6 +382,27 @@ def test_diag_f16_and_bf16_rounding():
     assert np.array_equal(got, oracle.bf16_bits(v))
 
 
+def test_diag_div6_exhaustive_against_ieee_division():
+    """The kernels' t / 6 against correctly rounded division for every one of
+    the 2^32 float32 bit patterns.  Reference: the quotient in binary64 rounded
+    once to binary32.  That single rounding is exact here: t / 6 is either
+    representable or has a repeating 01 binary expansion, which is never
+    within 2^-52 of a binary32 midpoint, so neither the binary64 rounding
+    nor a reciprocal-multiply inside the double division can move it across
+    one."""
+    chunk = 1 << 28
+    mism = 0
+    for start in range(0, 1 << 32, chunk):
+        bits = torch.arange(start, start + chunk, dtype=torch.int64, device=DEV)
+        v = (bits - (bits >= 2 ** 31).to(torch.int64) * 2 ** 32).to(torch.int32).view(torch.float32)
+        out = torch.empty_like(v)
+        fos.diag_convert(fos.DIAG_DIV6, v, out)
+        ref = (v.double() / 6.0).float()
+        same = (out.view(torch.int32) == ref.view(torch.int32)) | (torch.isnan(out) & torch.isnan(ref))
+        mism += int((~same).sum().item())
+    assert mism == 0
+
+
 def test_diag_div6_is_correctly_rounded():
     v = _dense_f32(1 << 22, seed=3)
     got = _run_diag(fos.DIAG_DIV6, v, torch.float32).numpy()
