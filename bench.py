@@ -314,7 +314,8 @@ def run_fos(args):
     achieved = ALG_BYTES / (enc_ms / 1e3) / 1e9
     out["roofline"] = {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
                        "unit": "GB/s", "frac": round(achieved / peak, 4),
-                       "traffic": _profiled_traffic(), "kernel": "k_quant1x16<bf16,MSE,TENSOR>",
+                       "traffic": _profiled_traffic(),
+                       "kernel": "k_quant1x16_tensor<bf16, MSE exact, per-tensor>",
                        "launch_ms": round(enc_ms, 5), "peak_kind": peak_kind + " (burst copy)"}
     out["clocks"] = clock_summary
 

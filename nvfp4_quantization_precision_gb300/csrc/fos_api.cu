@@ -169,6 +169,40 @@ cudaError_t run_quant(const void* x, fos_dtype dt, int64_t rows, int64_t cols,
     return cudaErrorInvalidValue;
 }
 
+// One-pass row-scaled 1x16 quantize: a CTA per row, each thread holding up to
+// K = 2 blocks of the row in registers (rows of 2048 .. 8192 columns).
+// Returns 0 outside that range; the two-pass path (row amax, then encode)
+// is used there.
+int rowpass_k(int64_t nb) {
+    if (nb < 128) return 0;  // short rows would leave most of a CTA idle
+    if (nb <= kThreads) return 1;
+    if (nb <= 2 * kThreads) return 2;
+    return 0;
+}
+
+cudaError_t run_rowpass(const void* x, fos_dtype dt, int64_t rows, int64_t cols,
+                        const fos_config* cfg, float* amax, uint8_t* codes, uint8_t* scales,
+                        int k, cudaStream_t s) {
+    EncArgs a{};
+    a.x = x;
+    a.codes = codes;
+    a.scales = scales;
+    a.amax = amax;
+    a.rows = rows;
+    a.nb = cols / 16;
+    a.nblk = rows * a.nb;
+    a.six_bound = 6.0f * (float)cfg->e4m3_bound;
+    a.neg_zero = -0.0f;
+    a.amax_given = cfg->amax_is_input;
+    const Err em = err_of(cfg);
+    switch (in_of(dt)) {
+        case In::BF16: return launch_quant1x16_rowpass_bf16(em, k, a, s);
+        case In::F16: return launch_quant1x16_rowpass_f16(em, k, a, s);
+        case In::F32: return launch_quant1x16_rowpass_f32(em, k, a, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
 }  // namespace
 
 extern "C" {
@@ -229,6 +263,10 @@ fos_status fos_quantize(const void* x, fos_dtype dt, int64_t rows, int64_t cols,
     if (dev < 0) return FOS_ERR_INVALID_ARG;
     DeviceScope scope(dev);
     if (scope.st) return scope.st;
+    if (src == Src::ROW && cfg->block == FOS_BLOCK_1X16) {
+        const int k = rowpass_k(cols / 16);
+        if (k) return cuda_status(run_rowpass(x, dt, rows, cols, cfg, amax, codes, scales, k, s));
+    }
     if (!cfg->amax_is_input) {
         st = cuda_status(run_amax(x, dt, rows, cols, src, amax, nullptr, 0, s));
         if (st) return st;

@@ -185,6 +185,12 @@ __device__ __forceinline__ void ld256(const void* p, uint32_t* w) {
                    "=r"(w[6]), "=r"(w[7])
                  : "l"(p));
 }
+// Hint the memory system to bring [p, p + bytes) into L2 (bytes a multiple of
+// 16, p 16-byte aligned).  Nothing waits for it; a later load just finds the
+// data closer.
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
 __device__ __forceinline__ void st256(void* p, const uint32_t* w) {
     asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(w[0]),
                  "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
@@ -273,6 +279,13 @@ __device__ __forceinline__ void build_table(float2* tbl, float S, int lane) {
         tbl[c] = make_float2(r, d);
     }
     __syncwarp();
+}
+
+// One entry of the common-scale table (see build_table).
+__device__ __forceinline__ float2 table_entry(float S, int c) {
+    const float sig = e4m3_f32((uint32_t)c);
+    if (sig == 0.0f) return make_float2(0.0f, 0.0f);
+    return make_float2(fdiv(S, sig), fdiv(sig, S));
 }
 
 __device__ __forceinline__ uint32_t pack4(uint32_t b0, uint32_t b1, uint32_t b2, uint32_t b3) {
@@ -397,13 +410,27 @@ __device__ __forceinline__ uint32_t scale_codes(float amax, float S) {
 // Full 1x16 block: returns codes (2 words), the E4M3 scale byte, and with
 // OT != NONE the 8 output words of the selected candidate's decode.
 template <Err EM, Out OT>
+__device__ __forceinline__ void encode_block_amax(const uint64_t (&xp)[8], float block_amax,
+                                                  float S, const float2* tbl, uint64_t nz,
+                                                  uint32_t (&code)[2], uint32_t& scale,
+                                                  uint32_t (&out)[8]);
+
+template <Err EM, Out OT>
 __device__ __forceinline__ void encode_block(const uint64_t (&xp)[8], float S,
                                              const float2* tbl, uint64_t nz,
                                              uint32_t (&code)[2], uint32_t& scale,
                                              uint32_t (&out)[8]) {
+    encode_block_amax<EM, OT>(xp, seg_amax(xp), S, tbl, nz, code, scale, out);
+}
+
+template <Err EM, Out OT>
+__device__ __forceinline__ void encode_block_amax(const uint64_t (&xp)[8], float block_amax,
+                                                  float S, const float2* tbl, uint64_t nz,
+                                                  uint32_t (&code)[2], uint32_t& scale,
+                                                  uint32_t (&out)[8]) {
     // Block scales are non-negative, so their codes are below 0x80; the mask
     // only keeps the table index in range by construction.
-    const uint32_t sc = scale_codes(seg_amax(xp), S);
+    const uint32_t sc = scale_codes(block_amax, S);
     const uint32_t c6 = sc & 0xFFu;
     const float2 rd6 = tbl[c6 & 0x7Fu];
     if constexpr (EM == Err::STD) {

@@ -34,6 +34,7 @@ struct EncArgs {
     int64_t cpr;           // 32-block chunks per row (ROW / GROUP)
     float six_bound;       // 6 * E4M3 bound
     float neg_zero;        // -0.0f (run-time operand of mul2_nc)
+    int amax_given;        // row pass: amax is an input (else computed, written)
 };
 
 struct QdqTensor {
@@ -71,6 +72,12 @@ struct AmaxArgs {
     int64_t rows, nb, units;
 };
 
+__device__ __forceinline__ float warp_max_dev(float m) {
+#pragma unroll
+    for (int w = 16; w >= 1; w >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, w));
+    return m;
+}
+
 // Position of a (row, chunk) walk.
 struct RowChunk {
     int64_t row, chunk;
@@ -89,7 +96,9 @@ __device__ __forceinline__ void load_if(Raw<IT>& r, const char* p, bool v) {
 // in each step the grid sweeps one contiguous window of the tensor; every
 // lane loads its next block one step ahead.
 // ------------------------------------------------------------------------
-template <In IT, Err EM>
+constexpr int kTensorBuf = 2;  // register buffers of the per-tensor encode (prefetch depth + 1)
+
+template <In IT, Err EM, int kBuf = kTensorBuf>
 __global__ void __launch_bounds__(kThreads) k_quant1x16_tensor(const EncArgs a) {
     chain_wait();
     chain_release();
@@ -102,28 +111,36 @@ __global__ void __launch_bounds__(kThreads) k_quant1x16_tensor(const EncArgs a) 
     if (u >= a.units) return;
     constexpr int64_t kBytes = (IT == In::F32) ? 64 : 32;
     const char* xb = static_cast<const char*>(a.x);
-    // Two units per iteration with two register buffers (A: u, B: u + nw):
-    // each buffer is refilled one step ahead without register copies.
+    // kBuf register buffers rotate over consecutive grid-stride units: unit i
+    // lives in buffer i % kBuf and is loaded kBuf - 1 units before it is
+    // encoded.  The loop body is unrolled over the buffers so every index is
+    // static (no register copies, no local memory).
     const int64_t step = nw * 32;
-    int64_t b = u * 32 + lane;
-    Raw<IT> ra, rb;
-    load_if<IT>(ra, xb + b * kBytes, b < a.nblk);
+    const int64_t b0 = u * 32 + lane;
+    Raw<IT> buf[kBuf];
+#pragma unroll
+    for (int k = 0; k < kBuf - 1; ++k) {
+        const int64_t bk = b0 + k * step;
+        load_if<IT>(buf[k], xb + bk * kBytes, bk < a.nblk);
+    }
     const float S = global_scale(a.amax[0], a.six_bound);
     build_table(tbl, S, lane);
     uint32_t dummy[8];
-    auto encode = [&](const Raw<IT>& r, int64_t blk) {
-        uint64_t xp[8];
-        widen<IT>(r, xp);
-        uint32_t code[2], scale;
-        encode_block<EM, Out::NONE>(xp, S, tbl, nz, code, scale, dummy);
-        st64(a.codes + blk * 8, code[0], code[1]);
-        st8(a.scales + blk, scale);
-    };
-    for (; b < a.nblk + lane; b += 2 * step) {  // b - lane is the first block of the unit
-        load_if<IT>(rb, xb + (b + step) * kBytes, b + step < a.nblk);
-        if (b < a.nblk) encode(ra, b);
-        load_if<IT>(ra, xb + (b + 2 * step) * kBytes, b + 2 * step < a.nblk);
-        if (b + step < a.nblk) encode(rb, b + step);
+    for (int64_t b = b0; b < a.nblk + lane; b += kBuf * step) {  // b - lane: first block of unit
+#pragma unroll
+        for (int k = 0; k < kBuf; ++k) {
+            const int64_t bl = b + (k + kBuf - 1) * step;  // unit loaded now
+            load_if<IT>(buf[(k + kBuf - 1) % kBuf], xb + bl * kBytes, bl < a.nblk);
+            const int64_t bc = b + k * step;  // unit encoded now
+            if (bc < a.nblk) {
+                uint64_t xp[8];
+                widen<IT>(buf[k], xp);
+                uint32_t code[2], scale;
+                encode_block<EM, Out::NONE>(xp, S, tbl, nz, code, scale, dummy);
+                st64(a.codes + bc * 8, code[0], code[1]);
+                st8(a.scales + bc, scale);
+            }
+        }
     }
 }
 
@@ -197,6 +214,85 @@ __global__ void __launch_bounds__(kThreads) k_quant1x16(const EncArgs a) {
         cur = nxt;
         cc = nc;
         j = jn;
+    }
+}
+
+// ------------------------------------------------------------------------
+// 1x16 quantize with a per-row scale in one pass: one CTA per row at a time
+// (grid-stride over rows).  Each thread keeps its K blocks of the row in
+// registers; the row amax (when it is not given) is a CTA max-reduction and
+// is written out, the CTA builds the row's common-scale table, then encodes.
+// The next row is loaded before the current one is encoded.  Two barriers per
+// row: shared buffers are rewritten only after every thread passed the next
+// row's first barrier, i.e. finished reading them.
+// ------------------------------------------------------------------------
+template <In IT, Err EM, int K>
+__global__ void __launch_bounds__(kThreads) k_quant1x16_rowpass(const EncArgs a) {
+    chain_wait();
+    chain_release();
+    __shared__ float2 s_tbl[128];
+    __shared__ float s_red[kWarps];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint64_t nz = pk(a.neg_zero, a.neg_zero);
+    constexpr int64_t kBytes = (IT == In::F32) ? 64 : 32;
+    const char* xb = static_cast<const char*>(a.x);
+    float* amax_out = const_cast<float*>(a.amax);
+    int64_t row = blockIdx.x;
+    if (row >= a.rows) return;
+    Raw<IT> cur[K], nxt[K];
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+        const int64_t j = tid + (int64_t)k * kThreads;
+        load_if<IT>(cur[k], xb + (row * a.nb + j) * kBytes, j < a.nb);
+    }
+    uint32_t dummy[8];
+    for (; row < a.rows; row += gridDim.x) {
+        const int64_t rown = row + gridDim.x;
+#pragma unroll
+        for (int k = 0; k < K; ++k) {
+            const int64_t j = tid + (int64_t)k * kThreads;
+            load_if<IT>(nxt[k], xb + (rown * a.nb + j) * kBytes, rown < a.rows && j < a.nb);
+        }
+        float bam[K];
+        float m = 0.0f;
+#pragma unroll
+        for (int k = 0; k < K; ++k) {
+            uint64_t xp[8];
+            widen<IT>(cur[k], xp);
+            // blocks past the row end were not loaded and contribute nothing
+            bam[k] = (tid + (int64_t)k * kThreads < a.nb) ? seg_amax(xp) : 0.0f;
+            m = fmaxf(m, bam[k]);
+        }
+        float A;
+        if (a.amax_given) {
+            A = a.amax[row];
+            __syncthreads();
+        } else {
+            m = warp_max_dev(m);
+            if (lane == 0) s_red[warp] = m;
+            __syncthreads();
+            A = 0.0f;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) A = fmaxf(A, s_red[w]);
+            if (tid == 0) amax_out[row] = A;
+        }
+        const float S = global_scale(A, a.six_bound);
+        if (tid < 128) s_tbl[tid] = table_entry(S, tid);
+        __syncthreads();
+#pragma unroll
+        for (int k = 0; k < K; ++k) {
+            const int64_t j = tid + (int64_t)k * kThreads;
+            if (j < a.nb) {
+                uint64_t xp[8];
+                widen<IT>(cur[k], xp);
+                uint32_t code[2], scale;
+                encode_block_amax<EM, Out::NONE>(xp, bam[k], S, s_tbl, nz, code, scale, dummy);
+                const int64_t b = row * a.nb + j;
+                st64(a.codes + b * 8, code[0], code[1]);
+                st8(a.scales + b, scale);
+            }
+            cur[k] = nxt[k];
+        }
     }
 }
 

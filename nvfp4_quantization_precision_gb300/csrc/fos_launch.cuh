@@ -110,6 +110,9 @@ inline cudaError_t launch_persistent(Kernel kernel, const Args& a, int64_t units
 cudaError_t launch_quant1x16_bf16(Err, Src, const EncArgs&, cudaStream_t);
 cudaError_t launch_quant1x16_f16(Err, Src, const EncArgs&, cudaStream_t);
 cudaError_t launch_quant1x16_f32(Err, Src, const EncArgs&, cudaStream_t);
+cudaError_t launch_quant1x16_rowpass_bf16(Err, int k, const EncArgs&, cudaStream_t);
+cudaError_t launch_quant1x16_rowpass_f16(Err, int k, const EncArgs&, cudaStream_t);
+cudaError_t launch_quant1x16_rowpass_f32(Err, int k, const EncArgs&, cudaStream_t);
 cudaError_t launch_quant16x16_bf16(Err, Src, const EncArgs&, cudaStream_t);
 cudaError_t launch_quant16x16_f16(Err, Src, const EncArgs&, cudaStream_t);
 cudaError_t launch_quant16x16_f32(Err, Src, const EncArgs&, cudaStream_t);

@@ -34,4 +34,24 @@ cudaError_t launch_quant1x16_f16(Err em, Src src, const EncArgs& a, cudaStream_t
     return cudaErrorInvalidValue;
 }
 
+template <Err EM>
+static cudaError_t rowpass(int k, const EncArgs& a, cudaStream_t s) {
+    switch (k) {
+        case 1: return launch_persistent(k_quant1x16_rowpass<In::F16, EM, 1>, a, a.rows * kWarps, 0, s);
+        case 2: return launch_persistent(k_quant1x16_rowpass<In::F16, EM, 2>, a, a.rows * kWarps, 0, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_quant1x16_rowpass_f16(Err em, int k, const EncArgs& a, cudaStream_t s) {
+    switch (em) {
+        case Err::STD: return rowpass<Err::STD>(k, a, s);
+        case Err::MAE: return rowpass<Err::MAE>(k, a, s);
+        case Err::MSE: return rowpass<Err::MSE>(k, a, s);
+        case Err::MAE_H: return rowpass<Err::MAE_H>(k, a, s);
+        case Err::MSE_H: return rowpass<Err::MSE_H>(k, a, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
 }  // namespace fos

@@ -439,3 +439,16 @@ def test_activation_full_size_sampled():
                 oc, os_, _ = oracle.quantize(xs[rows].float().numpy(), ocfg2, amax=ref_a)
                 assert np.array_equal(gc.cpu().numpy()[rows], oc), (fam, mode, row)
                 assert np.array_equal(gs.cpu().numpy()[rows], os_), (fam, mode, row)
+
+
+# ------------------------------------------------------------------ one-pass row scale
+@pytest.mark.parametrize("dt", ["bf16", "f16", "f32"])
+@pytest.mark.parametrize("mode", list(MODES))
+@pytest.mark.parametrize("shape", [(5, 2048), (3, 4096), (9, 4800), (4, 7168), (2, 8192),
+                                   (300, 2064)])
+def test_row_scaled_one_pass_shapes(dt, mode, shape):
+    """Row lengths served by the one-pass row kernel (128..512 blocks per row,
+    ragged last thread, more rows than a CTA handles at once)."""
+    gcfg, ocfg = _cfgs(mode, 448 if mode != "mse_f16" else 256, True)
+    for i, fam in enumerate(("F2", "F4")):
+        _check_quant(_x(*shape, fam, seed=11 + i, dt=dt), gcfg, ocfg, amax_given=(i == 1))
