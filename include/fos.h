@@ -114,6 +114,38 @@ FOS_API fos_status fos_quantize(const void* x, fos_dtype dt, int64_t rows, int64
                         fos_stream_t stream);
 
 /*
+ * fos_quantize_list -- fos_quantize over a list of n tensors of one dtype
+ * and one configuration; entry i reads x[i] (rows[i] x cols[i]) and writes
+ * amax[i], codes[i], scales[i] exactly as fos_quantize would.  With 1x16
+ * blocks, per-tensor scale and the amax computed by the library, the work is
+ * pipelined: the amax pass of tensor i+1 runs in dedicated warps of the
+ * launch that encodes tensor i (the encode is bound by instruction issue,
+ * the amax pass by HBM reads), so a list costs about one amax pass plus n
+ * encodes.  Other configurations run the entries one after another.
+ * Host arrays must hold n entries; errors as for fos_quantize (the first
+ * failing entry's status, nothing launched).
+ */
+FOS_API fos_status fos_quantize_list(int n, const void* const* x, fos_dtype dt,
+                                     const int64_t* rows, const int64_t* cols,
+                                     const fos_config* cfg, float* const* amax,
+                                     uint8_t* const* codes, uint8_t* const* scales,
+                                     fos_stream_t stream);
+
+/*
+ * fos_quantize_overlap -- one stage of the list pipeline, for callers that
+ * pipeline their own tensors: quantize x (1x16 blocks, per-tensor scale,
+ * cfg->amax_is_input must be 1, amax given) and, in the same launch, compute
+ * the per-tensor amax of x_next (same dtype, rows_next x cols_next) into
+ * amax_next[0] (cleared first, written by the launch).  With amax_next NULL
+ * it is fos_quantize.  Returns FOS_ERR_UNSUPPORTED for other configurations.
+ */
+FOS_API fos_status fos_quantize_overlap(const void* x, fos_dtype dt, int64_t rows, int64_t cols,
+                                        const fos_config* cfg, const float* amax,
+                                        uint8_t* codes, uint8_t* scales, const void* x_next,
+                                        int64_t rows_next, int64_t cols_next,
+                                        float* amax_next, fos_stream_t stream);
+
+/*
  * fos_dequantize -- standard NVFP4 decode (grouped PR, first commit:
  * "nvfp4_dequantize: the standard NVFP4 decode (recipe-agnostic)"):
  *   out = round_to(out_dt, e2m1(code) * (e4m3(scale) / S)),

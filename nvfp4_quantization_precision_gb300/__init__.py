@@ -8,6 +8,8 @@ is not built, or a tensor is not on a CUDA device, the call raises.
 Entry points (names follow the C ABI):
   amax(x, granularity)                      -> float32 amax
   quantize(x, ...)                          -> (codes, scales, amax)
+  quantize_list(xs, ...)                    -> ([codes], [scales], [amax])
+  quantize_overlap(x, amax, codes, scales, x_next, amax_next)
   dequantize(codes, scales, amax, ...)      -> tensor
   qdq(xs, ...)                              -> list of tensors (one launch)
   quantize_grouped(x, offs, ...)            -> (codes, scales, group_amax)
@@ -27,7 +29,8 @@ QDQ_MAX_LIST = 64
 GROUPED_MAX_GROUPS = 8192
 
 _DT = {torch.bfloat16: FOS_BF16, torch.float16: FOS_FP16, torch.float32: FOS_FP32}
-_NAMES = ("fos_amax", "fos_quantize", "fos_dequantize", "fos_qdq", "fos_quantize_grouped",
+_NAMES = ("fos_amax", "fos_quantize", "fos_quantize_list", "fos_quantize_overlap",
+          "fos_dequantize", "fos_qdq", "fos_quantize_grouped",
           "fos_status_string", "fos_version", "fos_diag_convert")
 
 
@@ -74,11 +77,14 @@ def lib():
         CFG = ctypes.POINTER(FosConfig)
         L.fos_amax.argtypes = [P, I, I64, I64, I, P, P]
         L.fos_quantize.argtypes = [P, I, I64, I64, CFG, P, P, P, P]
+        L.fos_quantize_list.argtypes = [I, P, I, P, P, CFG, P, P, P, P]
+        L.fos_quantize_overlap.argtypes = [P, I, I64, I64, CFG, P, P, P, P, I64, I64, P, P]
         L.fos_dequantize.argtypes = [P, P, P, I64, I64, CFG, P, I, P]
         L.fos_qdq.argtypes = [I, P, P, P, P, P, I, CFG, P]
         L.fos_quantize_grouped.argtypes = [P, I, I64, I64, P, I, CFG, P, P, P, P]
         L.fos_diag_convert.argtypes = [I, P, P, I64, P]
-        for n in ("fos_amax", "fos_quantize", "fos_dequantize", "fos_qdq",
+        for n in ("fos_amax", "fos_quantize", "fos_quantize_list", "fos_quantize_overlap",
+                  "fos_dequantize", "fos_qdq",
                   "fos_quantize_grouped", "fos_diag_convert"):
             getattr(L, n).restype = ctypes.c_int
         L.fos_status_string.argtypes = [I]
@@ -147,6 +153,58 @@ def quantize(x, cfg=Config(), amax=None, codes=None, scales=None, amax_given=Non
     _check(lib().fos_quantize(_p(x), _DT[x.dtype], R, C, ctypes.byref(cc), _p(amax), _p(codes),
                               _p(scales), _stream(x)), "fos_quantize")
     return codes, scales, amax
+
+
+def quantize_list(xs, cfg=Config(), amaxes=None, codes=None, scales=None, amax_given=None):
+    """fos_quantize over a list of tensors of one dtype (see fos_quantize_list:
+    with per-tensor scale and amax computed, the amax pass of tensor i+1 runs
+    inside the encode launch of tensor i).  Returns (codes, scales, amaxes)
+    lists."""
+    n = len(xs)
+    if n == 0:
+        return [], [], []
+    for x in xs:
+        _cuda(x, "x")
+    dt = xs[0].dtype
+    given = (amaxes is not None) if amax_given is None else bool(amax_given)
+    dev = xs[0].device
+    if amaxes is None:
+        amaxes = [torch.empty(x.shape[0] if cfg.row_scaled else 1, dtype=torch.float32,
+                              device=dev) for x in xs]
+    if codes is None:
+        codes = [torch.empty((x.shape[0], x.shape[1] // 2), dtype=torch.uint8, device=dev)
+                 for x in xs]
+    if scales is None:
+        scales = [torch.empty(scales_shape(x.shape[0], x.shape[1], cfg.block16x16),
+                              dtype=torch.uint8, device=dev) for x in xs]
+    P = ctypes.c_void_p * n
+    xp = P(*[x.data_ptr() for x in xs])
+    ap = P(*[a.data_ptr() for a in amaxes])
+    cp = P(*[c.data_ptr() for c in codes])
+    sp = P(*[s.data_ptr() for s in scales])
+    rows = (ctypes.c_int64 * n)(*[x.shape[0] for x in xs])
+    cols = (ctypes.c_int64 * n)(*[x.shape[1] for x in xs])
+    cc = cfg.c(given)
+    _check(lib().fos_quantize_list(n, xp, _DT[dt], rows, cols, ctypes.byref(cc), ap, cp, sp,
+                                   _stream(xs[0])), "fos_quantize_list")
+    return codes, scales, amaxes
+
+
+def quantize_overlap(x, amax, codes, scales, x_next=None, amax_next=None, cfg=Config()):
+    """Quantize x with its per-tensor amax given (1x16) and compute the amax
+    of x_next in the same launch (fos_quantize_overlap)."""
+    _cuda(x, "x")
+    R, C = x.shape
+    if x_next is not None:
+        _cuda(x_next, "x_next")
+        Rn, Cn = x_next.shape
+    else:
+        Rn = Cn = 0
+    cc = cfg.c(True)
+    _check(lib().fos_quantize_overlap(_p(x), _DT[x.dtype], R, C, ctypes.byref(cc), _p(amax),
+                                      _p(codes), _p(scales), _p(x_next), Rn, Cn, _p(amax_next),
+                                      _stream(x)), "fos_quantize_overlap")
+    return codes, scales
 
 
 def dequantize(codes, scales, amax, cfg=Config(), out_dtype=torch.bfloat16, out=None):

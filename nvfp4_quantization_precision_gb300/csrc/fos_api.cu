@@ -8,6 +8,7 @@
 // the host.
 #include <cstdint>
 #include <cstring>
+#include <vector>
 
 #include "../../include/fos.h"
 #include "../../include/fos_diag.h"
@@ -111,10 +112,12 @@ fos_status cuda_status(cudaError_t e) {
 In in_of(fos_dtype dt) { return dt == FOS_BF16 ? In::BF16 : (dt == FOS_FP16 ? In::F16 : In::F32); }
 
 cudaError_t run_amax(const void* x, fos_dtype dt, int64_t rows, int64_t cols, Src scope,
-                     float* amax, const int32_t* offs, int G, cudaStream_t s) {
+                     float* amax, const int32_t* offs, int G, cudaStream_t s,
+                     float* clear = nullptr) {
     AmaxArgs a{};
     a.x = x;
     a.amax = amax;
+    a.clear = clear;
     a.offs = offs;
     a.G = G;
     a.rows = rows;
@@ -129,6 +132,23 @@ cudaError_t run_amax(const void* x, fos_dtype dt, int64_t rows, int64_t cols, Sr
     if (rows == 0) return cudaSuccess;
     if (cols == 0) return cudaMemsetAsync(amax, 0, sizeof(float) * (size_t)rows, s);
     return launch_amax(in_of(dt), scope, a, s);
+}
+
+// Per-tensor amax into a buffer that is already +0 (no memset).
+cudaError_t run_amax_cleared(const void* x, fos_dtype dt, int64_t rows, int64_t cols,
+                             float* amax, cudaStream_t s, float* clear = nullptr) {
+    AmaxArgs a{};
+    a.x = x;
+    a.amax = amax;
+    a.clear = clear;
+    a.rows = rows;
+    a.nb = cols / 16;
+    a.units = (rows * a.nb + 31) / 32;
+    if (rows == 0 || cols == 0) {
+        if (clear) return cudaMemsetAsync(clear, 0, sizeof(float), s);
+        return cudaSuccess;
+    }
+    return launch_amax(in_of(dt), Src::TENSOR, a, s);
 }
 
 cudaError_t run_quant(const void* x, fos_dtype dt, int64_t rows, int64_t cols,
@@ -203,6 +223,92 @@ cudaError_t run_rowpass(const void* x, fos_dtype dt, int64_t rows, int64_t cols,
     return cudaErrorInvalidValue;
 }
 
+// Encode x (1x16, per-tensor amax given) and, in the same launch, the amax
+// pass of x_next (cleared first).  Without x_next it is a plain encode.
+// With next_cleared the caller guarantees amax_next is already +0 (the list
+// clears it one stage earlier); clear_ahead, when set, is zeroed by this
+// launch for a later stage.
+fos_status overlap_one(const void* x, fos_dtype dt, int64_t rows, int64_t cols,
+                       const fos_config* cfg, const float* amax, uint8_t* codes, uint8_t* scales,
+                       const void* x_next, int64_t rows_next, int64_t cols_next, float* amax_next,
+                       cudaStream_t s, bool next_cleared = false, float* clear_ahead = nullptr) {
+    fos_status st = FOS_OK;
+    const bool next = amax_next != nullptr;
+    const bool next_live = next && rows_next > 0 && cols_next > 0;
+    if (clear_ahead && !(next_live && rows > 0 && cols > 0)) {
+        // this stage does not launch the overlapped kernel: clear directly
+        st = cuda_status(cudaMemsetAsync(clear_ahead, 0, sizeof(float), s));
+        if (st) return st;
+        clear_ahead = nullptr;
+    }
+    if (next && !next_cleared) {
+        st = cuda_status(cudaMemsetAsync(amax_next, 0, sizeof(float), s));
+        if (st) return st;
+    }
+    if (rows == 0 || cols == 0) {
+        if (next_live)
+            return cuda_status(run_amax_cleared(x_next, dt, rows_next, cols_next, amax_next, s));
+        return FOS_OK;
+    }
+    if (!next_live)
+        return cuda_status(run_quant(x, dt, rows, cols, cfg, amax, Src::TENSOR, nullptr, 0, codes,
+                                     scales, s));
+    PipeArgs p{};
+    EncArgs& a = p.enc;
+    a.x = x;
+    a.codes = codes;
+    a.scales = scales;
+    a.amax = amax;
+    a.rows = rows;
+    a.nb = cols / 16;
+    a.nblk = a.rows * a.nb;
+    a.units = (a.nblk + 31) / 32;
+    a.cpr = (a.nb + 31) / 32;
+    a.six_bound = 6.0f * (float)cfg->e4m3_bound;
+    a.neg_zero = -0.0f;
+    p.clear = clear_ahead;
+    p.ax = x_next;
+    p.aamax = amax_next;
+    p.aseg = rows_next * (cols_next / 16);
+    p.aunits = (p.aseg + 31) / 32;
+    return cuda_status(launch_pipe(in_of(dt), err_of(cfg), p, s));
+}
+
+// Shape / pointer / alignment checks of one quantize call (no CUDA calls).
+fos_status check_quant_args(const void* x, int64_t rows, int64_t cols, const fos_config* cfg,
+                            const float* amax, const uint8_t* codes, const uint8_t* scales) {
+    fos_status st = check_shape(rows, cols, cfg->block == FOS_BLOCK_16X16);
+    if (st) return st;
+    if (rows == 0 || cols == 0) {
+        if (!cfg->amax_is_input && !(cfg->granularity == FOS_SCALE_ROW && rows == 0) && !amax)
+            return FOS_ERR_INVALID_ARG;
+        return FOS_OK;
+    }
+    if (!x || !amax || !codes || !scales) return FOS_ERR_INVALID_ARG;
+    if (!aligned(x, 32) || !aligned(codes, 8)) return FOS_ERR_MISALIGNED;
+    return FOS_OK;
+}
+
+// One quantize on the current device (arguments already validated).
+fos_status quantize_one(const void* x, fos_dtype dt, int64_t rows, int64_t cols,
+                        const fos_config* cfg, float* amax, uint8_t* codes, uint8_t* scales,
+                        cudaStream_t s) {
+    const Src src = cfg->granularity == FOS_SCALE_ROW ? Src::ROW : Src::TENSOR;
+    if (rows == 0 || cols == 0) {  // nothing to encode; a computed amax is 0
+        const size_t n = (src == Src::ROW) ? (size_t)rows : 1;
+        return cuda_status(cudaMemsetAsync(amax, 0, sizeof(float) * n, s));
+    }
+    if (src == Src::ROW && cfg->block == FOS_BLOCK_1X16) {
+        const int k = rowpass_k(cols / 16);
+        if (k) return cuda_status(run_rowpass(x, dt, rows, cols, cfg, amax, codes, scales, k, s));
+    }
+    if (!cfg->amax_is_input) {
+        fos_status st = cuda_status(run_amax(x, dt, rows, cols, src, amax, nullptr, 0, s));
+        if (st) return st;
+    }
+    return cuda_status(run_quant(x, dt, rows, cols, cfg, amax, src, nullptr, 0, codes, scales, s));
+}
+
 }  // namespace
 
 extern "C" {
@@ -243,35 +349,112 @@ fos_status fos_quantize(const void* x, fos_dtype dt, int64_t rows, int64_t cols,
     if (!valid_dtype(dt)) return FOS_ERR_INVALID_ARG;
     fos_status st = check_config(cfg);
     if (st) return st;
-    st = check_shape(rows, cols, cfg->block == FOS_BLOCK_16X16);
+    st = check_quant_args(x, rows, cols, cfg, amax, codes, scales);
     if (st) return st;
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    const Src src = cfg->granularity == FOS_SCALE_ROW ? Src::ROW : Src::TENSOR;
-    if (rows == 0 || cols == 0) {  // nothing to encode; a computed amax is 0
-        if (cfg->amax_is_input || (src == Src::ROW && rows == 0)) return FOS_OK;
-        if (!amax) return FOS_ERR_INVALID_ARG;
-        const int d = device_of(amax);
-        if (d < 0) return FOS_ERR_INVALID_ARG;
-        DeviceScope scope(d);
-        if (scope.st) return scope.st;
-        const size_t n = (src == Src::ROW) ? (size_t)rows : 1;
-        return cuda_status(cudaMemsetAsync(amax, 0, sizeof(float) * n, s));
-    }
-    if (!x || !amax || !codes || !scales) return FOS_ERR_INVALID_ARG;
-    if (!aligned(x, 32) || !aligned(codes, 8)) return FOS_ERR_MISALIGNED;
-    const int dev = common_device({x, amax, codes, scales});
+    const bool empty = rows == 0 || cols == 0;
+    if (empty && (cfg->amax_is_input || (cfg->granularity == FOS_SCALE_ROW && rows == 0)))
+        return FOS_OK;  // nothing to read or write
+    const int dev = empty ? device_of(amax) : common_device({x, amax, codes, scales});
     if (dev < 0) return FOS_ERR_INVALID_ARG;
     DeviceScope scope(dev);
     if (scope.st) return scope.st;
-    if (src == Src::ROW && cfg->block == FOS_BLOCK_1X16) {
-        const int k = rowpass_k(cols / 16);
-        if (k) return cuda_status(run_rowpass(x, dt, rows, cols, cfg, amax, codes, scales, k, s));
+    return quantize_one(x, dt, rows, cols, cfg, amax, codes, scales,
+                        reinterpret_cast<cudaStream_t>(stream));
+}
+
+fos_status fos_quantize_overlap(const void* x, fos_dtype dt, int64_t rows, int64_t cols,
+                                const fos_config* cfg, const float* amax, uint8_t* codes,
+                                uint8_t* scales, const void* x_next, int64_t rows_next,
+                                int64_t cols_next, float* amax_next, fos_stream_t stream) {
+    if (!valid_dtype(dt)) return FOS_ERR_INVALID_ARG;
+    fos_status st = check_config(cfg);
+    if (st) return st;
+    if (cfg->block != FOS_BLOCK_1X16 || cfg->granularity != FOS_SCALE_TENSOR ||
+        !cfg->amax_is_input)
+        return FOS_ERR_UNSUPPORTED;
+    st = check_quant_args(x, rows, cols, cfg, amax, codes, scales);
+    if (st) return st;
+    if (amax_next) {
+        st = check_shape(rows_next, cols_next, false);
+        if (st) return st;
+        if (rows_next > 0 && cols_next > 0) {
+            if (!x_next) return FOS_ERR_INVALID_ARG;
+            if (!aligned(x_next, 32)) return FOS_ERR_MISALIGNED;
+        }
     }
-    if (!cfg->amax_is_input) {
-        st = cuda_status(run_amax(x, dt, rows, cols, src, amax, nullptr, 0, s));
+    const bool empty = rows == 0 || cols == 0;
+    const bool next_live = amax_next && rows_next > 0 && cols_next > 0;
+    int dev = -1;
+    if (!empty) dev = common_device({x, amax, codes, scales});
+    if (amax_next) {
+        const int d = next_live ? common_device({x_next, amax_next}) : device_of(amax_next);
+        if (d < 0 || (dev >= 0 && d != dev)) return FOS_ERR_INVALID_ARG;
+        dev = d;
+    }
+    if (dev < 0) return empty ? FOS_OK : FOS_ERR_INVALID_ARG;
+    DeviceScope scope(dev);
+    if (scope.st) return scope.st;
+    return overlap_one(x, dt, rows, cols, cfg, amax, codes, scales, x_next, rows_next, cols_next,
+                       amax_next, reinterpret_cast<cudaStream_t>(stream));
+}
+
+fos_status fos_quantize_list(int n, const void* const* x, fos_dtype dt, const int64_t* rows,
+                             const int64_t* cols, const fos_config* cfg, float* const* amax,
+                             uint8_t* const* codes, uint8_t* const* scales,
+                             fos_stream_t stream) {
+    if (n < 0) return FOS_ERR_INVALID_ARG;
+    if (!valid_dtype(dt)) return FOS_ERR_INVALID_ARG;
+    fos_status st = check_config(cfg);
+    if (st) return st;
+    if (n == 0) return FOS_OK;
+    if (!x || !rows || !cols || !amax || !codes || !scales) return FOS_ERR_INVALID_ARG;
+    for (int i = 0; i < n; ++i) {  // host-side checks of every entry first
+        st = check_quant_args(x[i], rows[i], cols[i], cfg, amax[i], codes[i], scales[i]);
         if (st) return st;
     }
-    return cuda_status(run_quant(x, dt, rows, cols, cfg, amax, src, nullptr, 0, codes, scales, s));
+    int dev = -1;
+    for (int i = 0; i < n; ++i) {
+        const bool empty = rows[i] == 0 || cols[i] == 0;
+        if (empty && !amax[i]) continue;
+        const int d = empty ? device_of(amax[i])
+                            : common_device({x[i], amax[i], codes[i], scales[i]});
+        if (d < 0 || (dev >= 0 && d != dev)) return FOS_ERR_INVALID_ARG;
+        dev = d;
+    }
+    if (dev < 0) return FOS_OK;  // only empty tensors with nothing to write
+    DeviceScope scope(dev);
+    if (scope.st) return scope.st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const bool pipelined = cfg->block == FOS_BLOCK_1X16 && cfg->granularity == FOS_SCALE_TENSOR &&
+                           !cfg->amax_is_input;
+    if (!pipelined) {
+        for (int i = 0; i < n; ++i) {
+            const bool empty = rows[i] == 0 || cols[i] == 0;
+            if (empty && (cfg->amax_is_input || (cfg->granularity == FOS_SCALE_ROW && rows[i] == 0)))
+                continue;
+            st = quantize_one(x[i], dt, rows[i], cols[i], cfg, amax[i], codes[i], scales[i], s);
+            if (st) return st;
+        }
+        return FOS_OK;
+    }
+    // Pipelined per-tensor path: amax(0); then for each i one launch that
+    // encodes tensor i and runs the amax pass of tensor i+1.  Every launch
+    // clears the amax buffer of the stage after the next one, so only the
+    // first buffer needs a memset and the launches chain back to back.
+    st = cuda_status(cudaMemsetAsync(amax[0], 0, sizeof(float), s));
+    if (st) return st;
+    st = cuda_status(run_amax_cleared(x[0], dt, rows[0], cols[0], amax[0], s,
+                                      n > 1 ? amax[1] : nullptr));
+    if (st) return st;
+    for (int i = 0; i < n; ++i) {
+        const bool more = i + 1 < n;
+        st = overlap_one(x[i], dt, rows[i], cols[i], cfg, amax[i], codes[i], scales[i],
+                         more ? x[i + 1] : nullptr, more ? rows[i + 1] : 0,
+                         more ? cols[i + 1] : 0, more ? amax[i + 1] : nullptr, s,
+                         /*next_cleared=*/true, i + 2 < n ? amax[i + 2] : nullptr);
+        if (st) return st;
+    }
+    return FOS_OK;
 }
 
 fos_status fos_quantize_grouped(const void* x, fos_dtype dt, int64_t rows, int64_t cols,

@@ -67,6 +67,7 @@ struct DeqArgs {
 struct AmaxArgs {
     const void* x;
     float* amax;
+    float* clear;          // optional: set to +0 by the launch (a later stage's amax)
     const int32_t* offs;
     int G;
     int64_t rows, nb, units;
@@ -438,6 +439,93 @@ __global__ void __launch_bounds__(kThreads) k_quant16x16(const EncArgs a) {
 }
 
 // ------------------------------------------------------------------------
+// List pipeline: one launch encodes tensor i (per-tensor scale, 1x16) and,
+// in separate warps of the same CTAs, runs the amax pass of tensor i+1.  The
+// encode is bound by instruction issue and leaves HBM bandwidth idle; the
+// amax pass is a pure read.  The kernel boundary orders amax(i+1) before
+// encode(i+1), so no grid-wide synchronisation is needed.  The amax target
+// must be +0 on entry (the host clears it before the launch).
+// ------------------------------------------------------------------------
+constexpr int kPipeEncWarps = 6;  // warps 0..5 encode, warps 6..7 run the amax pass
+
+struct PipeArgs {
+    EncArgs enc;           // tensor i (amax given)
+    float* clear;          // optional: set to +0 by the launch (amax of tensor i+2)
+    const void* ax;        // tensor i+1: input
+    float* aamax;          //             amax output (cleared)
+    int64_t aseg;          //             16-element segments
+    int64_t aunits;        //             32-segment units
+};
+
+template <In IT, Err EM>
+__global__ void __launch_bounds__(kThreads) k_quant1x16_pipe(const PipeArgs p) {
+    chain_wait();
+    chain_release();
+    if (p.clear && blockIdx.x == 0 && threadIdx.x == 0) *p.clear = 0.0f;
+    __shared__ float2 s_tbl[kPipeEncWarps][128];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    constexpr int64_t kBytes = (IT == In::F32) ? 64 : 32;
+    if (warp >= kPipeEncWarps) {
+        // amax pass of the next tensor: four units in flight per lane
+        constexpr int kAmaxWarps = kWarps - kPipeEncWarps;
+        const int64_t nw = (int64_t)gridDim.x * kAmaxWarps;
+        const char* xb = static_cast<const char*>(p.ax);
+        float m = 0.0f;
+        for (int64_t u = (int64_t)blockIdx.x * kAmaxWarps + (warp - kPipeEncWarps); u < p.aunits;
+             u += 4 * nw) {
+            Raw<IT> r[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int64_t sg = (u + k * nw) * 32 + lane;
+                zero_seg<IT>(r[k]);
+                if (u + k * nw < p.aunits && sg < p.aseg) load_seg<IT>(r[k], xb + sg * kBytes);
+            }
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                uint64_t xp[8];
+                widen<IT>(r[k], xp);
+                m = fmaxf(m, seg_amax(xp));
+            }
+        }
+        m = warp_max_dev(m);
+        if (lane == 0 && m > 0.0f)
+            atomicMax(reinterpret_cast<unsigned int*>(p.aamax), __float_as_uint(m));
+        return;
+    }
+    // encode of the current tensor: grid-stride over 32-block units
+    const EncArgs& a = p.enc;
+    float2* tbl = s_tbl[warp];
+    const uint64_t nz = pk(a.neg_zero, a.neg_zero);
+    const int64_t nw = (int64_t)gridDim.x * kPipeEncWarps;
+    const int64_t u = (int64_t)blockIdx.x * kPipeEncWarps + warp;
+    if (u >= a.units) return;
+    const char* xb = static_cast<const char*>(a.x);
+    const int64_t step = nw * 32;
+    const int64_t b0 = u * 32 + lane;
+    Raw<IT> buf[2];
+    load_if<IT>(buf[0], xb + b0 * kBytes, b0 < a.nblk);
+    const float S = global_scale(a.amax[0], a.six_bound);
+    build_table(tbl, S, lane);
+    uint32_t dummy[8];
+    for (int64_t b = b0; b < a.nblk + lane; b += 2 * step) {
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const int64_t bl = b + (k + 1) * step;
+            load_if<IT>(buf[(k + 1) % 2], xb + bl * kBytes, bl < a.nblk);
+            const int64_t bc = b + k * step;
+            if (bc < a.nblk) {
+                uint64_t xp[8];
+                widen<IT>(buf[k], xp);
+                uint32_t code[2], scale;
+                encode_block<EM, Out::NONE>(xp, S, tbl, nz, code, scale, dummy);
+                st64(a.codes + bc * 8, code[0], code[1]);
+                st8(a.scales + bc, scale);
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------------------
 // Dequantize: out = round_to(OT, e2m1(code) * (sigma / S)).
 // Unit = (row, 32-block chunk).  B16: 16x16 scale layout.
 // ------------------------------------------------------------------------
@@ -511,6 +599,7 @@ template <In IT>
 __global__ void __launch_bounds__(kThreads) k_amax_tensor(const AmaxArgs a) {
     chain_wait();
     chain_release();
+    if (a.clear && blockIdx.x == 0 && threadIdx.x == 0) *a.clear = 0.0f;
     __shared__ float s_m[kWarps];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t nw = (int64_t)gridDim.x * kWarps;

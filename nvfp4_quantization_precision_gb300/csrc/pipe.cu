@@ -1,0 +1,32 @@
+// Instantiations of the list pipeline kernel (encode of tensor i with the
+// amax pass of tensor i+1 in the same launch).
+#include "fos_launch.cuh"
+
+namespace fos {
+
+template <In IT>
+static cudaError_t by_err(Err em, const PipeArgs& a, cudaStream_t s) {
+    // units = the larger of the two roles' needs, in warps of that role
+    const int64_t enc_w = (a.enc.units + kPipeEncWarps - 1) / kPipeEncWarps;
+    const int64_t am_w = (a.aunits + (kWarps - kPipeEncWarps) - 1) / (kWarps - kPipeEncWarps);
+    const int64_t units = (enc_w > am_w ? enc_w : am_w) * kWarps;
+    switch (em) {
+        case Err::STD: return launch_persistent(k_quant1x16_pipe<IT, Err::STD>, a, units, 0, s);
+        case Err::MAE: return launch_persistent(k_quant1x16_pipe<IT, Err::MAE>, a, units, 0, s);
+        case Err::MSE: return launch_persistent(k_quant1x16_pipe<IT, Err::MSE>, a, units, 0, s);
+        case Err::MAE_H: return launch_persistent(k_quant1x16_pipe<IT, Err::MAE_H>, a, units, 0, s);
+        case Err::MSE_H: return launch_persistent(k_quant1x16_pipe<IT, Err::MSE_H>, a, units, 0, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_pipe(In it, Err em, const PipeArgs& a, cudaStream_t s) {
+    switch (it) {
+        case In::BF16: return by_err<In::BF16>(em, a, s);
+        case In::F16: return by_err<In::F16>(em, a, s);
+        case In::F32: return by_err<In::F32>(em, a, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace fos

@@ -29,7 +29,8 @@ def _declared():
 
 def test_headers_declare_the_entry_points():
     d = _declared()
-    for n in ("fos_amax", "fos_quantize", "fos_dequantize", "fos_qdq", "fos_quantize_grouped",
+    for n in ("fos_amax", "fos_quantize", "fos_quantize_list", "fos_quantize_overlap",
+              "fos_dequantize", "fos_qdq", "fos_quantize_grouped",
               "fos_status_string", "fos_version", "fos_diag_convert"):
         assert n in d
 
@@ -145,3 +146,31 @@ def test_python_binding_refuses_cpu_tensors():
     import torch
     with pytest.raises(ValueError):
         fos.quantize(torch.zeros(16, 16, dtype=torch.bfloat16))
+
+
+def test_quantize_list_rejects_before_launching(L):
+    P = ctypes.c_void_p * 2
+    xs, am, cs, ss = P(FAKE.value, FAKE.value), P(FAKE.value, FAKE.value), \
+        P(FAKE.value, FAKE.value), P(FAKE.value, FAKE.value)
+    rows = (ctypes.c_int64 * 2)(16, 16)
+    cols = (ctypes.c_int64 * 2)(16, 24)  # the second entry is invalid
+    c = _cfg(amax_is_input=0)
+    assert L.fos_quantize_list(2, xs, 0, rows, cols, ctypes.byref(c), am, cs, ss, None) == \
+        fos.FOS_ERR_UNSUPPORTED
+    assert L.fos_quantize_list(-1, xs, 0, rows, cols, ctypes.byref(c), am, cs, ss, None) == \
+        fos.FOS_ERR_INVALID_ARG
+    assert L.fos_quantize_list(0, None, 0, None, None, ctypes.byref(c), None, None, None,
+                               None) == fos.FOS_OK
+
+
+def test_quantize_overlap_requires_given_per_tensor_1x16(L):
+    for kw in (dict(block=1), dict(granularity=1), dict(amax_is_input=0)):
+        c = _cfg(**kw)
+        assert L.fos_quantize_overlap(FAKE, 0, 16, 16, ctypes.byref(c), FAKE, FAKE, FAKE, FAKE,
+                                      16, 16, FAKE, None) == fos.FOS_ERR_UNSUPPORTED
+    c = _cfg()
+    assert L.fos_quantize_overlap(FAKE, 0, 16, 16, ctypes.byref(c), FAKE, FAKE, FAKE,
+                                  ctypes.c_void_p(0x10010), 16, 16, FAKE, None) == \
+        fos.FOS_ERR_MISALIGNED
+    assert L.fos_quantize_overlap(FAKE, 0, 16, 16, ctypes.byref(c), FAKE, FAKE, FAKE, FAKE,
+                                  16, 20, FAKE, None) == fos.FOS_ERR_UNSUPPORTED

@@ -452,3 +452,57 @@ def test_row_scaled_one_pass_shapes(dt, mode, shape):
     gcfg, ocfg = _cfgs(mode, 448 if mode != "mse_f16" else 256, True)
     for i, fam in enumerate(("F2", "F4")):
         _check_quant(_x(*shape, fam, seed=11 + i, dt=dt), gcfg, ocfg, amax_given=(i == 1))
+
+
+# ------------------------------------------------------------------ quantize list
+@pytest.mark.parametrize("dt", ["bf16", "f16", "f32"])
+@pytest.mark.parametrize("mode", list(MODES))
+@pytest.mark.parametrize("row", [False, True])
+def test_quantize_list(dt, mode, row):
+    """fos_quantize_list equals the oracle entry by entry; with per-tensor
+    scale and amax computed it runs the pipelined launches (empty and ragged
+    entries included)."""
+    gcfg, ocfg = _cfgs(mode, 448, row)
+    shapes = [(64, 1024), (0, 64), (7, 1040), (256, 2048), (48, 272), (1, 16)]
+    xs = [_x(r, c, fam, i, dt) if r else torch.zeros(0, c, dtype=DTYPES[dt])
+          for i, ((r, c), fam) in enumerate(zip(shapes, workloads.FAMILIES * 2))]
+    gc, gs, ga = fos.quantize_list([x.to(DEV) for x in xs], gcfg)
+    torch.cuda.synchronize()
+    for x, c, s_, a in zip(xs, gc, gs, ga):
+        if x.numel() == 0:
+            if not row:
+                assert float(a[0]) == 0.0
+            continue
+        oc, os_, oa = oracle.quantize(x.float().numpy(), ocfg)
+        assert np.array_equal(_u32(a), oa.view(np.uint32))
+        assert np.array_equal(s_.cpu().numpy(), os_)
+        assert np.array_equal(c.cpu().numpy(), oc)
+
+
+def test_quantize_list_equals_single_calls_full_size():
+    gcfg, _ = _cfgs("mse")
+    xs = [workloads.activation(8192, 4096, f, seed=i, device=DEV)
+          for i, f in enumerate(workloads.FAMILIES)]
+    gc, gs, ga = fos.quantize_list(xs, gcfg)
+    for x, c, s_, a in zip(xs, gc, gs, ga):
+        c1, s1, a1 = fos.quantize(x, gcfg)
+        torch.cuda.synchronize()
+        assert torch.equal(a, a1) and torch.equal(c, c1) and torch.equal(s_, s1)
+
+
+@pytest.mark.parametrize("mode", list(MODES))
+def test_quantize_overlap_stage(mode):
+    gcfg, ocfg = _cfgs(mode)
+    x = _x(96, 2048, "F2", 21, "bf16")
+    xn = _x(40, 528, "F4", 22, "bf16")
+    xf, xnf = x.float().numpy(), xn.float().numpy()
+    a = torch.from_numpy(oracle.amax_tensor(xf)).to(DEV)
+    an = torch.full((1,), 123.0, device=DEV)  # overwritten by the call
+    c = torch.empty(96, 1024, dtype=torch.uint8, device=DEV)
+    s_ = torch.empty(96, 128, dtype=torch.uint8, device=DEV)
+    fos.quantize_overlap(x.to(DEV), a, c, s_, xn.to(DEV), an, gcfg)
+    torch.cuda.synchronize()
+    ocfg2 = oracle.Config(**{**ocfg.__dict__, "amax_is_input": True})
+    oc, os_, _ = oracle.quantize(xf, ocfg2, amax=a.cpu().numpy())
+    assert np.array_equal(c.cpu().numpy(), oc) and np.array_equal(s_.cpu().numpy(), os_)
+    assert np.array_equal(_u32(an), oracle.amax_tensor(xnf).view(np.uint32))
