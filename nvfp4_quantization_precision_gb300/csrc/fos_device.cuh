@@ -185,6 +185,30 @@ __device__ __forceinline__ void ld256(const void* p, uint32_t* w) {
                    "=r"(w[6]), "=r"(w[7])
                  : "l"(p));
 }
+// L2 eviction priority of a load: NORMAL, FIRST (streamed, last use) or LAST
+// (read again soon).
+enum class L2 : int { NORMAL = 0, FIRST = 1, LAST = 2 };
+template <L2 H>
+__device__ __forceinline__ uint64_t l2_policy() {
+    uint64_t pol;
+    if constexpr (H == L2::FIRST)
+        asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    else
+        asm("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+template <L2 H>
+__device__ __forceinline__ void ld256h(const void* p, uint32_t* w) {
+    if constexpr (H == L2::NORMAL) {
+        ld256(p, w);
+    } else {
+        asm volatile(
+            "ld.global.nc.L1::no_allocate.L2::cache_hint.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8], %9;"
+            : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]), "=r"(w[6]),
+              "=r"(w[7])
+            : "l"(p), "l"(l2_policy<H>()));
+    }
+}
 // Hint the memory system to bring [p, p + bytes) into L2 (bytes a multiple of
 // 16, p 16-byte aligned).  Nothing waits for it; a later load just finds the
 // data closer.
@@ -209,10 +233,10 @@ struct Raw {
     uint32_t w[InTraits<IT>::kWords];
 };
 
-template <In IT>
+template <In IT, L2 H = L2::NORMAL>
 __device__ __forceinline__ void load_seg(Raw<IT>& r, const void* p) {
-    ld256(p, r.w);
-    if constexpr (IT == In::F32) ld256(static_cast<const char*>(p) + 32, r.w + 8);
+    ld256h<H>(p, r.w);
+    if constexpr (IT == In::F32) ld256h<H>(static_cast<const char*>(p) + 32, r.w + 8);
 }
 
 template <In IT>

@@ -87,10 +87,21 @@ struct RowChunk {
     }
 };
 
-template <In IT>
+template <In IT, L2 H = L2::NORMAL>
 __device__ __forceinline__ void load_if(Raw<IT>& r, const char* p, bool v) {
-    if (v) load_seg<IT>(r, p);
+    if (v) load_seg<IT, H>(r, p);
 }
+
+// L2 priorities of the per-tensor paths.
+constexpr L2 kEncHint = L2::FIRST;    // encode loads (read once)
+constexpr L2 kAmaxHint = L2::NORMAL;  // amax-pass loads
+constexpr L2 kQdqHint = L2::NORMAL;   // fused QDQ loads
+// Minimum resident CTAs per SM the encode kernels are compiled for: caps
+// their registers at 65536 / (256 * n).
+constexpr int kStdMinCtas = 5;
+constexpr int kFosMinCtas = 4;
+template <Err EM>
+constexpr int min_ctas() { return EM == Err::STD ? kStdMinCtas : kFosMinCtas; }
 
 // ------------------------------------------------------------------------
 // 1x16 quantize with a per-tensor scale.  Grid-stride over 32-block units:
@@ -100,7 +111,7 @@ __device__ __forceinline__ void load_if(Raw<IT>& r, const char* p, bool v) {
 constexpr int kTensorBuf = 2;  // register buffers of the per-tensor encode (prefetch depth + 1)
 
 template <In IT, Err EM, int kBuf = kTensorBuf>
-__global__ void __launch_bounds__(kThreads) k_quant1x16_tensor(const EncArgs a) {
+__global__ void __launch_bounds__(kThreads, min_ctas<EM>()) k_quant1x16_tensor(const EncArgs a) {
     chain_wait();
     chain_release();
     __shared__ float2 s_tbl[kWarps][128];
@@ -122,7 +133,7 @@ __global__ void __launch_bounds__(kThreads) k_quant1x16_tensor(const EncArgs a) 
 #pragma unroll
     for (int k = 0; k < kBuf - 1; ++k) {
         const int64_t bk = b0 + k * step;
-        load_if<IT>(buf[k], xb + bk * kBytes, bk < a.nblk);
+        load_if<IT, kEncHint>(buf[k], xb + bk * kBytes, bk < a.nblk);
     }
     const float S = global_scale(a.amax[0], a.six_bound);
     build_table(tbl, S, lane);
@@ -131,7 +142,7 @@ __global__ void __launch_bounds__(kThreads) k_quant1x16_tensor(const EncArgs a) 
 #pragma unroll
         for (int k = 0; k < kBuf; ++k) {
             const int64_t bl = b + (k + kBuf - 1) * step;  // unit loaded now
-            load_if<IT>(buf[(k + kBuf - 1) % kBuf], xb + bl * kBytes, bl < a.nblk);
+            load_if<IT, kEncHint>(buf[(k + kBuf - 1) % kBuf], xb + bl * kBytes, bl < a.nblk);
             const int64_t bc = b + k * step;  // unit encoded now
             if (bc < a.nblk) {
                 uint64_t xp[8];
@@ -151,7 +162,7 @@ __global__ void __launch_bounds__(kThreads) k_quant1x16_tensor(const EncArgs a) 
 // (and its table) changes only at row / group boundaries.
 // ------------------------------------------------------------------------
 template <In IT, Err EM, Src SRC>
-__global__ void __launch_bounds__(kThreads) k_quant1x16(const EncArgs a) {
+__global__ void __launch_bounds__(kThreads, min_ctas<EM>()) k_quant1x16(const EncArgs a) {
     chain_wait();
     chain_release();
     extern __shared__ int32_t s_ends[];
@@ -170,7 +181,7 @@ __global__ void __launch_bounds__(kThreads) k_quant1x16(const EncArgs a) {
     RowChunk cc{u0 / a.cpr, u0 % a.cpr};
     int64_t j = cc.chunk * 32 + lane;
     Raw<IT> cur;
-    load_if<IT>(cur, xb + (cc.row * a.nb + j) * kBytes, j < a.nb && cc.row < last_end);
+    load_if<IT, kEncHint>(cur, xb + (cc.row * a.nb + j) * kBytes, j < a.nb && cc.row < last_end);
     int g = 0;
     if constexpr (SRC == Src::GROUP)
         while (g < a.G && cc.row >= s_ends[g]) ++g;
@@ -182,7 +193,7 @@ __global__ void __launch_bounds__(kThreads) k_quant1x16(const EncArgs a) {
         nc.next(a.cpr);
         const int64_t jn = nc.chunk * 32 + lane;
         Raw<IT> nxt;
-        load_if<IT>(nxt, xb + (nc.row * a.nb + jn) * kBytes,
+        load_if<IT, kEncHint>(nxt, xb + (nc.row * a.nb + jn) * kBytes,
                     u + 1 < u1 && jn < a.nb && nc.row < last_end);
         int64_t k;
         if constexpr (SRC == Src::ROW) {
@@ -244,7 +255,7 @@ __global__ void __launch_bounds__(kThreads) k_quant1x16_rowpass(const EncArgs a)
 #pragma unroll
     for (int k = 0; k < K; ++k) {
         const int64_t j = tid + (int64_t)k * kThreads;
-        load_if<IT>(cur[k], xb + (row * a.nb + j) * kBytes, j < a.nb);
+        load_if<IT, kEncHint>(cur[k], xb + (row * a.nb + j) * kBytes, j < a.nb);
     }
     uint32_t dummy[8];
     for (; row < a.rows; row += gridDim.x) {
@@ -252,7 +263,7 @@ __global__ void __launch_bounds__(kThreads) k_quant1x16_rowpass(const EncArgs a)
 #pragma unroll
         for (int k = 0; k < K; ++k) {
             const int64_t j = tid + (int64_t)k * kThreads;
-            load_if<IT>(nxt[k], xb + (rown * a.nb + j) * kBytes, rown < a.rows && j < a.nb);
+            load_if<IT, kEncHint>(nxt[k], xb + (rown * a.nb + j) * kBytes, rown < a.rows && j < a.nb);
         }
         float bam[K];
         float m = 0.0f;
@@ -305,7 +316,7 @@ __global__ void __launch_bounds__(kThreads) k_quant1x16_rowpass(const EncArgs a)
 // warp's unit moves into the next tensor.
 // ------------------------------------------------------------------------
 template <In IT, Err EM>
-__global__ void __launch_bounds__(kThreads) k_qdq1x16(const __grid_constant__ QdqArgs a) {
+__global__ void __launch_bounds__(kThreads, min_ctas<EM>()) k_qdq1x16(const __grid_constant__ QdqArgs a) {
     chain_wait();
     chain_release();
     static_assert(IT != In::F32, "fused QDQ is bf16 / fp16 only");
@@ -322,7 +333,7 @@ __global__ void __launch_bounds__(kThreads) k_qdq1x16(const __grid_constant__ Qd
     int64_t b = (u - a.t[t].unit_begin) * 32 + lane;
     bool v = b < a.t[t].nblk;
     Raw<IT> cur;
-    load_if<IT>(cur, static_cast<const char*>(a.t[t].x) + b * 32, v);
+    load_if<IT, kQdqHint>(cur, static_cast<const char*>(a.t[t].x) + b * 32, v);
     int ti = -1;
     float S = 1.0f;
     for (; u < a.units; u += nw) {
@@ -332,7 +343,7 @@ __global__ void __launch_bounds__(kThreads) k_qdq1x16(const __grid_constant__ Qd
         const int64_t bn = (un - a.t[tn].unit_begin) * 32 + lane;
         const bool vn = un < a.units && bn < a.t[tn].nblk;
         Raw<IT> nxt;
-        load_if<IT>(nxt, static_cast<const char*>(a.t[tn].x) + bn * 32, vn);
+        load_if<IT, kQdqHint>(nxt, static_cast<const char*>(a.t[tn].x) + bn * 32, vn);
         if (t != ti) {
             ti = t;
             S = global_scale(*a.t[t].amax, a.six_bound);
@@ -358,7 +369,7 @@ __global__ void __launch_bounds__(kThreads) k_qdq1x16(const __grid_constant__ Qd
 // per warp, next unit loaded one step ahead.
 // ------------------------------------------------------------------------
 template <In IT, Err EM, Src SRC>
-__global__ void __launch_bounds__(kThreads) k_quant16x16(const EncArgs a) {
+__global__ void __launch_bounds__(kThreads, min_ctas<EM>()) k_quant16x16(const EncArgs a) {
     chain_wait();
     chain_release();
     extern __shared__ int32_t s_ends[];
@@ -381,7 +392,7 @@ __global__ void __launch_bounds__(kThreads) k_quant16x16(const EncArgs a) {
         const int64_t J = p.chunk * 2 + half;
         zero_seg<IT>(r);
         if (in_range && J < a.nb && p.row * 16 < last_end)
-            load_seg<IT>(r, xb + ((p.row * 16 + r16) * cols + J * 16) * kElt);
+            load_seg<IT, kEncHint>(r, xb + ((p.row * 16 + r16) * cols + J * 16) * kElt);
     };
     Raw<IT> cur;
     load_unit(cur, cc, true);
@@ -458,7 +469,7 @@ struct PipeArgs {
 };
 
 template <In IT, Err EM>
-__global__ void __launch_bounds__(kThreads) k_quant1x16_pipe(const PipeArgs p) {
+__global__ void __launch_bounds__(kThreads, min_ctas<EM>()) k_quant1x16_pipe(const PipeArgs p) {
     chain_wait();
     chain_release();
     if (p.clear && blockIdx.x == 0 && threadIdx.x == 0) *p.clear = 0.0f;
@@ -478,7 +489,7 @@ __global__ void __launch_bounds__(kThreads) k_quant1x16_pipe(const PipeArgs p) {
             for (int k = 0; k < 4; ++k) {
                 const int64_t sg = (u + k * nw) * 32 + lane;
                 zero_seg<IT>(r[k]);
-                if (u + k * nw < p.aunits && sg < p.aseg) load_seg<IT>(r[k], xb + sg * kBytes);
+                if (u + k * nw < p.aunits && sg < p.aseg) load_seg<IT, kAmaxHint>(r[k], xb + sg * kBytes);
             }
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
@@ -503,7 +514,7 @@ __global__ void __launch_bounds__(kThreads) k_quant1x16_pipe(const PipeArgs p) {
     const int64_t step = nw * 32;
     const int64_t b0 = u * 32 + lane;
     Raw<IT> buf[2];
-    load_if<IT>(buf[0], xb + b0 * kBytes, b0 < a.nblk);
+    load_if<IT, kEncHint>(buf[0], xb + b0 * kBytes, b0 < a.nblk);
     const float S = global_scale(a.amax[0], a.six_bound);
     build_table(tbl, S, lane);
     uint32_t dummy[8];
@@ -511,7 +522,7 @@ __global__ void __launch_bounds__(kThreads) k_quant1x16_pipe(const PipeArgs p) {
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
             const int64_t bl = b + (k + 1) * step;
-            load_if<IT>(buf[(k + 1) % 2], xb + bl * kBytes, bl < a.nblk);
+            load_if<IT, kEncHint>(buf[(k + 1) % 2], xb + bl * kBytes, bl < a.nblk);
             const int64_t bc = b + k * step;
             if (bc < a.nblk) {
                 uint64_t xp[8];
@@ -613,8 +624,8 @@ __global__ void __launch_bounds__(kThreads) k_amax_tensor(const AmaxArgs a) {
         Raw<IT> r0, r1;
         zero_seg<IT>(r0);
         zero_seg<IT>(r1);
-        if (s0 < nseg) load_seg<IT>(r0, xb + s0 * kBytes);
-        if (u + nw < a.units && s1 < nseg) load_seg<IT>(r1, xb + s1 * kBytes);
+        if (s0 < nseg) load_seg<IT, kAmaxHint>(r0, xb + s0 * kBytes);
+        if (u + nw < a.units && s1 < nseg) load_seg<IT, kAmaxHint>(r1, xb + s1 * kBytes);
         uint64_t xp[8];
         widen<IT>(r0, xp);
         m = fmaxf(m, seg_amax(xp));
