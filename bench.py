@@ -4,9 +4,8 @@ Workload (one step): the activation batch of four 8192 x 4096 bf16 tensors,
 one per input family (F1 N(0,1), F2 with 0.1 % x100 outliers, F3 U(-1,1),
 F4 with 25 % zero / tiny blocks), each quantized four-over-six with 1x16
 blocks, a per-tensor FP32 amax computed on the device, E4M3 bound 448 and
-MSE with exact-FP32 candidate error.  A step runs the amax pass of all four
-tensors, then the encode of all four, so the encode reads its input from HBM
-(the four inputs total 256 MiB, twice the L2).
+MSE with exact-FP32 candidate error.  The four inputs total 256 MiB, twice
+the L2, so every pass reads its input from HBM.
 
 `value` is whole-job HBM throughput in GB/s counting the algorithmic bytes
 once per tensor (read 2 B + write 0.5 B codes + 1/16 B scale per element);
@@ -14,8 +13,9 @@ the amax pass's second read of x is not counted, so the figure is strict.
 The step is the pipelined list quantize (fos_quantize_list's launches): the
 amax pass of tensor 0, then one launch per tensor that encodes it while
 other warps run the amax pass of the next tensor.  `roofline` is that
-overlapped launch (average of the three inside the timed region; its
-algorithmic bytes are the encode's plus the next tensor's read).  `e2e` repeats the step through the same C-ABI calls starting from
+overlapped launch (timed in its own loop of the three stages; its
+algorithmic bytes are the encode's plus the next tensor's read).  `e2e`
+repeats the step through the same C-ABI calls starting from
 pinned host buffers, with the host->device copy of the inputs and the
 device->host copy of codes and scales inside the timed region.
 
@@ -151,6 +151,39 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------- helpers
+def max_over_ranks(x, dev):
+    """The largest of a per-rank float over the default process group (the
+    float itself without one)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def step_line(ms, ws, steps, warmup, peak):
+    """The bench line's step fields from the slowest rank's time per step:
+    every rank quantizes its own four tensors (replicas, weak scaling), so the
+    whole job moves ws * 4 tensors per step."""
+    units = ws * 4
+    value = units * ALG_BYTES / (ms / 1e3) / 1e9
+    return {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws,
+        "steps": steps, "warmup": warmup, "ms_per_step": round(ms, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded families F1-F4, generated on device)",
+        "config": {"workload": WORKLOAD, "tensors_per_step_per_gpu": 4,
+                   "l2": "inputs larger than L2: 4 x 64 MiB per step, 2x the 129 MB L2",
+                   "bytes_per_tensor": ALG_BYTES, "launch": "CUDA graph replay of C-ABI calls",
+                   "parallelism": "replicas x%d" % ws},
+        "pct_of_peak": round(100.0 * value / ws / peak, 2),
+        "elements_per_s": round(units * ELEMS / (ms / 1e3), 1),
+        "gpu_launches": 5 * steps,
+    }
+
+
 def _dist():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -292,25 +325,8 @@ def run_fos(args):
     g_st.replay()
     pipe_ms = _time_events(g_st.replay, max(3, args.steps // 4), stream) / 3
     clock_summary = clocks.summary(t_wall0, t_wall1)
-    if ws > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-
-    units = ws * 4  # tensors processed per step, all ranks
-    value = units * ALG_BYTES / (ms / 1e3) / 1e9
-    out = {
-        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-        "data": "synthetic (seeded families F1-F4, generated on device)",
-        "config": {"workload": WORKLOAD, "tensors_per_step_per_gpu": 4,
-                   "l2": "inputs larger than L2: 4 x 64 MiB per step, 2x the 129 MB L2",
-                   "bytes_per_tensor": ALG_BYTES, "launch": "CUDA graph replay of C-ABI calls"},
-        "pct_of_peak": round(100.0 * value / ws / peak, 2),
-        "elements_per_s": round(units * ELEMS / (ms / 1e3), 1),
-        "gpu_launches": 5 * args.steps,
-    }
+    ms = max_over_ranks(ms, dev)
+    out = step_line(ms, ws, args.steps, args.warmup, peak)
     pipe_bytes = ALG_BYTES + ELEMS * 2  # encode of tensor i + amax read of tensor i+1
     achieved = pipe_bytes / (pipe_ms / 1e3) / 1e9
     out["roofline"] = {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
@@ -321,13 +337,14 @@ def run_fos(args):
                        "launch_ms": round(pipe_ms, 5), "peak_kind": peak_kind + " (burst copy)"}
     out["clocks"] = clock_summary
 
+    if not args.skip_extras:
+        out["e2e"] = _e2e(fos, xs, cfg, stream, args, ws, dev)
     if rank == 0 and ws == 1 and not args.skip_extras:
         # the same step as one eager fos_quantize_list call (host time included)
         def eager():
             fos.quantize_list(xs, cfg, amaxes=amax, codes=codes, scales=scales, amax_given=False)
         eager()
         out["eager_ms_per_step"] = round(_time_events(eager, max(5, args.steps // 4), stream), 5)
-        out["e2e"] = _e2e(fos, xs, cfg, stream, args)
         out["rows"] = _rows(fos, xs, stream, peak)
         out["cpu_baseline"] = _cpu_baseline(args.cpu_seconds)
     clocks.stop()
@@ -337,7 +354,7 @@ def run_fos(args):
         print(json.dumps(out))
 
 
-def _e2e(fos, xs, cfg, stream, args):
+def _e2e(fos, xs, cfg, stream, args, ws, dev):
     """The step from pinned host buffers through the public API: H2D of the
     four inputs, amax + encode (fos_quantize computes the amax), D2H of codes
     and scales, all inside the timed region."""
@@ -362,10 +379,10 @@ def _e2e(fos, xs, cfg, stream, args):
     reps = max(3, args.steps // 10)
     for _ in range(3):
         step()
-    ms = _time_events(step, reps, stream)
+    ms = max_over_ranks(_time_events(step, reps, stream), dev)
     h2d = 4 * ELEMS * 2
     d2h = 4 * (ELEMS // 2 + ELEMS // 16)
-    return {"value": round(4 * ALG_BYTES / (ms / 1e3) / 1e9, 2), "unit": "GB/s",
+    return {"value": round(ws * 4 * ALG_BYTES / (ms / 1e3) / 1e9, 2), "unit": "GB/s",
             "ms_per_step": round(ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "steps": reps}
 
@@ -465,7 +482,24 @@ def _rows(fos, xs, stream, peak):
         esz = 2 if dt == torch.bfloat16 else 4
         rec("weight_16x16_14336x4096_" + ("bf16" if esz == 2 else "fp32"),
             14336 * 4096 * (esz + 0.5 + 1 / 256), ms)
+        if dt == torch.bfloat16:
+            wo = torch.empty(14336, 4096, dtype=torch.bfloat16, device=dev)
+            ms = _graph_ms(lambda: fos.dequantize(wc, wsc, wa, c, out=wo), 4, stream)
+            rec("weight_16x16_dequantize_bf16", 14336 * 4096 * (0.5 + 1 / 256 + 2), ms)
+            del wo
         del w
+    # expert stack 64 x 2048x7168 bf16, 16x16 tiles, one flattened call with
+    # each expert's amax expanded to its rows
+    E, ER, EC = 64, 2048, 7168
+    xe = workloads.moe_experts(E, ER, EC, seed=0, device=dev).view(E * ER, EC)
+    ea = torch.stack([fos.amax(xe[e * ER:(e + 1) * ER])[0] for e in range(E)])
+    ra_e = ea.repeat_interleave(ER)
+    c = fos.Config(block16x16=True, row_scaled=True)
+    ec = torch.empty(E * ER, EC // 2, dtype=torch.uint8, device=dev)
+    es = torch.empty(E * ER // 16, EC // 16, dtype=torch.uint8, device=dev)
+    ms = _graph_ms(lambda: fos.quantize(xe, c, amax=ra_e, codes=ec, scales=es), 2, stream)
+    rec("experts_16x16_64x2048x7168_bf16", E * ER * EC * (2 + 0.5 + 1 / 256), ms)
+    del xe, ec, es
     return res
 
 
