@@ -170,7 +170,7 @@ cudaError_t run_quant(const void* x, fos_dtype dt, int64_t rows, int64_t cols,
     const Err em = err_of(cfg);
     const In it = in_of(dt);
     if (cfg->block == FOS_BLOCK_16X16) {
-        a.cpr = (a.nb + 1) / 2;  // tile pairs per 16-row band
+        a.cpr = (a.nb + 3) / 4;  // tile quads per 16-row band
         a.units = (rows / 16) * a.cpr;
         switch (it) {
             case In::BF16: return launch_quant16x16_bf16(em, src, a, s);

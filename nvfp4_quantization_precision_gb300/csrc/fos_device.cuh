@@ -477,43 +477,55 @@ __device__ __forceinline__ void encode_block_amax(const uint64_t (&xp)[8], float
     }
 }
 
-// 16x16 tile: each of 16 lanes (a half-warp) holds one 16-element row of the
-// tile.  The tile amax is a NaN-dropping max across the half-warp; each
-// lane's row error is its width-16 tree, and the tile error runs the same
-// tree over the 16 row partials (lane i adds lane i+w for w = 8,4,2,1).
-__device__ __forceinline__ float half_max(float m) {
-#pragma unroll
-    for (int w = 8; w >= 1; w >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, w));
-    return m;
+// 16x16 tile over lanes: lane l holds rows r = l >> 2 and r + 8 of tile
+// t = l & 3, so the 16 rows of a tile sit in lanes t, t + 4, ..., t + 28.
+// The tile amax is a NaN-dropping max over those lanes.  The tile error is
+// the pinned tree over the 16 row partials (for w = 8,4,2,1: t[i] +=
+// t[i+w]); level w = 8 pairs the two rows a lane holds, levels 4, 2, 1 pair
+// lanes 16, 8 and 4 apart, and lane t ends with the tile's sum.
+__device__ __forceinline__ float quad_max(float m) {
+    m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 4));
+    m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 8));
+    return fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 16));
 }
-__device__ __forceinline__ float half_tree(float p) {
-#pragma unroll
-    for (int w = 8; w >= 1; w >>= 1) p = fadd(p, __shfl_down_sync(0xFFFFFFFFu, p, w, 16));
-    return __shfl_sync(0xFFFFFFFFu, p, 0, 16);
+__device__ __forceinline__ float quad_tree(float p_r, float p_r8, int t) {
+    float q = fadd(p_r, p_r8);
+    q = fadd(q, __shfl_down_sync(0xFFFFFFFFu, q, 16));
+    q = fadd(q, __shfl_down_sync(0xFFFFFFFFu, q, 8));
+    q = fadd(q, __shfl_down_sync(0xFFFFFFFFu, q, 4));
+    return __shfl_sync(0xFFFFFFFFu, q, t);
 }
 
+// Both rows (r, r + 8) a lane holds of one 16x16 tile: codes of each row and
+// the tile's E4M3 scale byte.  Every lane of the warp must take part.
 template <Err EM>
-__device__ __forceinline__ void encode_tile_row(const uint64_t (&xp)[8], float S,
-                                                const float2* tbl, uint64_t nz,
-                                                uint32_t (&code)[2], uint32_t& scale) {
-    const uint32_t sc = scale_codes(half_max(seg_amax(xp)), S);
+__device__ __forceinline__ void encode_tile_rows(const uint64_t (&x0)[8], const uint64_t (&x1)[8],
+                                                 float S, const float2* tbl, uint64_t nz, int t,
+                                                 uint32_t (&k0)[2], uint32_t (&k1)[2],
+                                                 uint32_t& scale) {
+    const uint32_t sc = scale_codes(quad_max(fmaxf(seg_amax(x0), seg_amax(x1))), S);
     const uint32_t c6 = sc & 0xFFu;
     const float2 rd6 = tbl[c6 & 0x7Fu];
     uint32_t dummy[8];
     if constexpr (EM == Err::STD) {
-        candidate<EM, Out::NONE>(xp, rd6.x, rd6.y, nz, code, dummy);
+        candidate<EM, Out::NONE>(x0, rd6.x, rd6.y, nz, k0, dummy);
+        candidate<EM, Out::NONE>(x1, rd6.x, rd6.y, nz, k1, dummy);
         scale = c6;
     } else {
         const uint32_t c4 = sc >> 8;
         const float2 rd4 = tbl[c4 & 0x7Fu];
-        uint32_t code6[2], code4[2];
-        const float e6 =
-            half_tree(candidate<EM, Out::NONE>(xp, rd6.x, rd6.y, nz, code6, dummy));
-        const float e4 =
-            half_tree(candidate<EM, Out::NONE>(xp, rd4.x, rd4.y, nz, code4, dummy));
+        uint32_t a0[2], a1[2], b0[2], b1[2];
+        const float p6 = candidate<EM, Out::NONE>(x0, rd6.x, rd6.y, nz, a0, dummy);
+        const float p6h = candidate<EM, Out::NONE>(x1, rd6.x, rd6.y, nz, a1, dummy);
+        const float e6 = quad_tree(p6, p6h, t);
+        const float p4 = candidate<EM, Out::NONE>(x0, rd4.x, rd4.y, nz, b0, dummy);
+        const float p4h = candidate<EM, Out::NONE>(x1, rd4.x, rd4.y, nz, b1, dummy);
+        const float e4 = quad_tree(p4, p4h, t);
         const bool sel4 = e4 < e6;
-        code[0] = sel4 ? code4[0] : code6[0];
-        code[1] = sel4 ? code4[1] : code6[1];
+        k0[0] = sel4 ? b0[0] : a0[0];
+        k0[1] = sel4 ? b0[1] : a0[1];
+        k1[0] = sel4 ? b1[0] : a1[0];
+        k1[1] = sel4 ? b1[1] : a1[1];
         scale = sel4 ? c4 : c6;
     }
 }

@@ -102,6 +102,10 @@ constexpr int kStdMinCtas = 5;
 constexpr int kFosMinCtas = 4;
 template <Err EM>
 constexpr int min_ctas() { return EM == Err::STD ? kStdMinCtas : kFosMinCtas; }
+// 16x16 (two rows per lane and the next two in flight): 80 registers for
+// 16-bit inputs, 128 for fp32.
+template <In IT>
+constexpr int tile_min_ctas() { return IT == In::F32 ? 2 : 3; }
 
 // ------------------------------------------------------------------------
 // 1x16 quantize with a per-tensor scale.  Grid-stride over 32-block units:
@@ -364,12 +368,15 @@ __global__ void __launch_bounds__(kThreads, min_ctas<EM>()) k_qdq1x16(const __gr
 }
 
 // ------------------------------------------------------------------------
-// 16x16 quantize.  Unit = (band of 16 rows, pair of 16x16 tiles); lane l
-// holds row (l & 15) of tile (2 * pair + (l >> 4)).  Contiguous unit range
-// per warp, next unit loaded one step ahead.
+// 16x16 quantize.  Unit = (band of 16 rows, quad of four 16x16 tiles); lane l
+// holds rows (l >> 2) and (l >> 2) + 8 of tile 4 * quad + (l & 3), so each
+// warp load reads eight whole 4-tile row spans.  Each CTA takes a contiguous
+// range of units and its warps interleave inside it (neighbouring warps read
+// neighbouring spans; the band, and with it a per-row or per-group scale,
+// changes rarely for any one warp).  The next unit is loaded one step ahead.
 // ------------------------------------------------------------------------
 template <In IT, Err EM, Src SRC>
-__global__ void __launch_bounds__(kThreads, min_ctas<EM>()) k_quant16x16(const EncArgs a) {
+__global__ void __launch_bounds__(kThreads, tile_min_ctas<IT>()) k_quant16x16(const EncArgs a) {
     chain_wait();
     chain_release();
     extern __shared__ int32_t s_ends[];
@@ -378,24 +385,28 @@ __global__ void __launch_bounds__(kThreads, min_ctas<EM>()) k_quant16x16(const E
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     float2* tbl = s_tbl[warp];
     const uint64_t nz = pk(a.neg_zero, a.neg_zero);
-    const int64_t nw = (int64_t)gridDim.x * kWarps, gw = (int64_t)blockIdx.x * kWarps + warp;
-    const int64_t u0 = split_at(a.units, nw, gw), u1 = split_at(a.units, nw, gw + 1);
-    if (u0 >= u1) return;
+    const int64_t c1 = split_at(a.units, gridDim.x, blockIdx.x + 1);
+    const int64_t u0 = split_at(a.units, gridDim.x, blockIdx.x) + warp;
+    if (u0 >= c1) return;
     constexpr int64_t kElt = (IT == In::F32) ? 4 : 2;
     const char* xb = static_cast<const char*>(a.x);
-    const int half = lane >> 4, r16 = lane & 15;
+    const int t = lane & 3, r = lane >> 2;
     const int64_t cols = a.nb * 16;
     int64_t last_end = a.rows;
     if constexpr (SRC == Src::GROUP) last_end = s_ends[a.G - 1];
-    RowChunk cc{u0 / a.cpr, u0 % a.cpr};  // row = band, chunk = tile pair
-    auto load_unit = [&](Raw<IT>& r, const RowChunk& p, bool in_range) {
-        const int64_t J = p.chunk * 2 + half;
-        zero_seg<IT>(r);
-        if (in_range && J < a.nb && p.row * 16 < last_end)
-            load_seg<IT, kEncHint>(r, xb + ((p.row * 16 + r16) * cols + J * 16) * kElt);
+    RowChunk cc{u0 / a.cpr, u0 % a.cpr};  // row = band, chunk = tile quad
+    auto load_unit = [&](Raw<IT>& lo, Raw<IT>& hi, const RowChunk& p, bool in_range) {
+        const int64_t J = p.chunk * 4 + t;
+        zero_seg<IT>(lo);
+        zero_seg<IT>(hi);
+        if (in_range && J < a.nb && p.row * 16 < last_end) {
+            const char* q = xb + ((p.row * 16 + r) * cols + J * 16) * kElt;
+            load_seg<IT, kEncHint>(lo, q);
+            load_seg<IT, kEncHint>(hi, q + 8 * cols * kElt);
+        }
     };
-    Raw<IT> cur;
-    load_unit(cur, cc, true);
+    Raw<IT> cur0, cur1;
+    load_unit(cur0, cur1, cc, true);
     int g = 0;
     if constexpr (SRC == Src::GROUP)
         while (g < a.G && cc.row * 16 >= s_ends[g]) ++g;
@@ -405,11 +416,15 @@ __global__ void __launch_bounds__(kThreads, min_ctas<EM>()) k_quant16x16(const E
         S = global_scale(a.amax[0], a.six_bound);
         build_table(tbl, S, lane);
     }
-    for (int64_t u = u0; u < u1; ++u) {
-        RowChunk nc = cc;
-        nc.next(a.cpr);
-        Raw<IT> nxt;
-        load_unit(nxt, nc, u + 1 < u1);
+    for (int64_t u = u0; u < c1; u += kWarps) {
+        RowChunk nc = cc;  // this warp's next unit, kWarps units on
+        nc.chunk += kWarps;
+        while (nc.chunk >= a.cpr) {
+            nc.chunk -= a.cpr;
+            ++nc.row;
+        }
+        Raw<IT> nxt0, nxt1;
+        load_unit(nxt0, nxt1, nc, u + kWarps < c1);
         const int64_t band = cc.row;
         bool tail = false;
         if constexpr (SRC != Src::TENSOR) {
@@ -429,22 +444,27 @@ __global__ void __launch_bounds__(kThreads, min_ctas<EM>()) k_quant16x16(const E
                 }
             }
         }
-        const int64_t J = cc.chunk * 2 + half;
-        const int64_t row = band * 16 + r16;
+        const int64_t J = cc.chunk * 4 + t;
+        uint8_t* c0 = a.codes + (band * 16 + r) * (cols / 2) + J * 8;
+        uint8_t* c8 = c0 + 8 * (cols / 2);
         if (!tail) {
-            uint64_t xp[8];
-            widen<IT>(cur, xp);  // zeros for a missing second tile
-            uint32_t code[2], scale;
-            encode_tile_row<EM>(xp, S, tbl, nz, code, scale);  // all lanes take part
+            uint64_t x0[8], x1[8];
+            widen<IT>(cur0, x0);  // zeros past the last tile of the band
+            widen<IT>(cur1, x1);
+            uint32_t k0[2], k1[2], scale;
+            encode_tile_rows<EM>(x0, x1, S, tbl, nz, t, k0, k1, scale);  // all lanes take part
             if (J < a.nb) {
-                st64(a.codes + row * (cols / 2) + J * 8, code[0], code[1]);
-                if (r16 == 0) st8(a.scales + band * a.nb + J, scale);
+                st64(c0, k0[0], k0[1]);
+                st64(c8, k1[0], k1[1]);
+                if (r == 0) st8(a.scales + band * a.nb + J, scale);
             }
         } else if (J < a.nb) {
-            st64(a.codes + row * (cols / 2) + J * 8, 0u, 0u);
-            if (r16 == 0) st8(a.scales + band * a.nb + J, 0u);
+            st64(c0, 0u, 0u);
+            st64(c8, 0u, 0u);
+            if (r == 0) st8(a.scales + band * a.nb + J, 0u);
         }
-        cur = nxt;
+        cur0 = nxt0;
+        cur1 = nxt1;
         cc = nc;
     }
 }
