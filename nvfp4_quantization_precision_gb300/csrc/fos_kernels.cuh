@@ -470,15 +470,17 @@ __global__ void __launch_bounds__(kThreads, tile_min_ctas<IT>()) k_quant16x16(co
 }
 
 // ------------------------------------------------------------------------
-// List pipeline: one launch encodes tensor i (per-tensor scale, 1x16) and,
-// in separate warps of the same CTAs, runs the amax pass of tensor i+1.  The
-// encode is bound by instruction issue and leaves HBM bandwidth idle; the
-// amax pass is a pure read.  The kernel boundary orders amax(i+1) before
-// encode(i+1), so no grid-wide synchronisation is needed.  The amax target
-// must be +0 on entry (the host clears it before the launch).
+// List pipeline: one launch encodes tensor i (per-tensor scale, 1x16) and
+// runs the amax pass of tensor i+1.  Every warp walks both tensors with the
+// same grid stride: in each step it loads one unit of tensor i+1, encodes
+// its unit of tensor i (whose load went out a step earlier) and then folds
+// the tensor i+1 unit into its running max, so that load's latency hides
+// behind the encode.  The encode is bound by instruction issue and leaves
+// HBM bandwidth idle; the extra read and max cost about 4 % more
+// instructions.  The kernel boundary orders amax(i+1) before encode(i+1),
+// so no grid-wide synchronisation is needed.  The amax target must be +0 on
+// entry (the host clears it before the launch).
 // ------------------------------------------------------------------------
-constexpr int kPipeEncWarps = 6;  // warps 0..5 encode, warps 6..7 run the amax pass
-
 struct PipeArgs {
     EncArgs enc;           // tensor i (amax given)
     float* clear;          // optional: set to +0 by the launch (amax of tensor i+2)
@@ -493,57 +495,34 @@ __global__ void __launch_bounds__(kThreads, min_ctas<EM>()) k_quant1x16_pipe(con
     chain_wait();
     chain_release();
     if (p.clear && blockIdx.x == 0 && threadIdx.x == 0) *p.clear = 0.0f;
-    __shared__ float2 s_tbl[kPipeEncWarps][128];
+    __shared__ float2 s_tbl[kWarps][128];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     constexpr int64_t kBytes = (IT == In::F32) ? 64 : 32;
-    if (warp >= kPipeEncWarps) {
-        // amax pass of the next tensor: four units in flight per lane
-        constexpr int kAmaxWarps = kWarps - kPipeEncWarps;
-        const int64_t nw = (int64_t)gridDim.x * kAmaxWarps;
-        const char* xb = static_cast<const char*>(p.ax);
-        float m = 0.0f;
-        for (int64_t u = (int64_t)blockIdx.x * kAmaxWarps + (warp - kPipeEncWarps); u < p.aunits;
-             u += 4 * nw) {
-            Raw<IT> r[4];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int64_t sg = (u + k * nw) * 32 + lane;
-                zero_seg<IT>(r[k]);
-                if (u + k * nw < p.aunits && sg < p.aseg) load_seg<IT, kAmaxHint>(r[k], xb + sg * kBytes);
-            }
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                uint64_t xp[8];
-                widen<IT>(r[k], xp);
-                m = fmaxf(m, seg_amax(xp));
-            }
-        }
-        m = warp_max_dev(m);
-        if (lane == 0 && m > 0.0f)
-            atomicMax(reinterpret_cast<unsigned int*>(p.aamax), __float_as_uint(m));
-        return;
-    }
-    // encode of the current tensor: grid-stride over 32-block units
     const EncArgs& a = p.enc;
     float2* tbl = s_tbl[warp];
     const uint64_t nz = pk(a.neg_zero, a.neg_zero);
-    const int64_t nw = (int64_t)gridDim.x * kPipeEncWarps;
-    const int64_t u = (int64_t)blockIdx.x * kPipeEncWarps + warp;
-    if (u >= a.units) return;
+    const int64_t nw = (int64_t)gridDim.x * kWarps;
+    const int64_t u = (int64_t)blockIdx.x * kWarps + warp;
     const char* xb = static_cast<const char*>(a.x);
+    const char* ab = static_cast<const char*>(p.ax);
     const int64_t step = nw * 32;
-    const int64_t b0 = u * 32 + lane;
+    const int64_t b0 = u * 32 + lane;  // this lane's block of tensor i, segment of tensor i+1
+    const int64_t nmax = a.nblk > p.aseg ? a.nblk : p.aseg;
     Raw<IT> buf[2];
     load_if<IT, kEncHint>(buf[0], xb + b0 * kBytes, b0 < a.nblk);
     const float S = global_scale(a.amax[0], a.six_bound);
     build_table(tbl, S, lane);
     uint32_t dummy[8];
-    for (int64_t b = b0; b < a.nblk + lane; b += 2 * step) {
+    float m = 0.0f;
+    for (int64_t b = b0; b < nmax + lane; b += 2 * step) {  // b - lane: first block of unit
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
             const int64_t bl = b + (k + 1) * step;
             load_if<IT, kEncHint>(buf[(k + 1) % 2], xb + bl * kBytes, bl < a.nblk);
             const int64_t bc = b + k * step;
+            Raw<IT> ra;
+            zero_seg<IT>(ra);
+            if (bc < p.aseg) load_seg<IT, kAmaxHint>(ra, ab + bc * kBytes);
             if (bc < a.nblk) {
                 uint64_t xp[8];
                 widen<IT>(buf[k], xp);
@@ -552,8 +531,14 @@ __global__ void __launch_bounds__(kThreads, min_ctas<EM>()) k_quant1x16_pipe(con
                 st64(a.codes + bc * 8, code[0], code[1]);
                 st8(a.scales + bc, scale);
             }
+            uint64_t xq[8];
+            widen<IT>(ra, xq);
+            m = fmaxf(m, seg_amax(xq));
         }
     }
+    m = warp_max_dev(m);
+    if (lane == 0 && m > 0.0f)
+        atomicMax(reinterpret_cast<unsigned int*>(p.aamax), __float_as_uint(m));
 }
 
 // ------------------------------------------------------------------------

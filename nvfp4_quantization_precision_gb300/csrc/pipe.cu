@@ -6,10 +6,8 @@ namespace fos {
 
 template <In IT>
 static cudaError_t by_err(Err em, const PipeArgs& a, cudaStream_t s) {
-    // units = the larger of the two roles' needs, in warps of that role
-    const int64_t enc_w = (a.enc.units + kPipeEncWarps - 1) / kPipeEncWarps;
-    const int64_t am_w = (a.aunits + (kWarps - kPipeEncWarps) - 1) / (kWarps - kPipeEncWarps);
-    const int64_t units = (enc_w > am_w ? enc_w : am_w) * kWarps;
+    // every warp walks both tensors: the larger unit count sizes the grid
+    const int64_t units = a.enc.units > a.aunits ? a.enc.units : a.aunits;
     switch (em) {
         case Err::STD: return launch_persistent(k_quant1x16_pipe<IT, Err::STD>, a, units, 0, s);
         case Err::MAE: return launch_persistent(k_quant1x16_pipe<IT, Err::MAE>, a, units, 0, s);
