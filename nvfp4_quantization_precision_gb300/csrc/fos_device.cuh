@@ -137,27 +137,6 @@ __device__ __forceinline__ uint64_t f16x2_f32x2(uint32_t h) {
         : "=f"(lo), "=f"(hi) : "r"(h));
     return pk(lo, hi);
 }
-// Exact widening through the mixed-precision add: v + (-0) is v.  The -0
-// comes from a register the compiler cannot see into, so the add is kept.
-__device__ __forceinline__ uint32_t opaque_neg_zero() {
-    uint32_t z;
-    asm volatile("mov.b32 %0, 0x80000000;" : "=r"(z));
-    return z;
-}
-__device__ __forceinline__ uint64_t f16x2_f32x2_add(uint32_t h, uint32_t nzb) {
-    float lo, hi;
-    asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\tadd.rn.f32.f16 %0, a, %3;\n\t"
-        "add.rn.f32.f16 %1, b, %3;\n\t}"
-        : "=f"(lo), "=f"(hi) : "r"(h), "f"(__uint_as_float(nzb)));
-    return pk(lo, hi);
-}
-__device__ __forceinline__ uint64_t bf16x2_f32x2_add(uint32_t w, uint32_t nzb) {
-    float lo, hi;
-    asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\tadd.rn.f32.bf16 %0, a, %3;\n\t"
-        "add.rn.f32.bf16 %1, b, %3;\n\t}"
-        : "=f"(lo), "=f"(hi) : "r"(w), "f"(__uint_as_float(nzb)));
-    return pk(lo, hi);
-}
 __device__ __forceinline__ uint32_t f32x2_f16x2(uint64_t p) {
     float lo, hi;
     upk(p, lo, hi);
