@@ -118,10 +118,11 @@ FOS_API fos_status fos_quantize(const void* x, fos_dtype dt, int64_t rows, int64
  * and one configuration; entry i reads x[i] (rows[i] x cols[i]) and writes
  * amax[i], codes[i], scales[i] exactly as fos_quantize would.  With 1x16
  * blocks, per-tensor scale and the amax computed by the library, the work is
- * pipelined: the amax pass of tensor i+1 runs in dedicated warps of the
- * launch that encodes tensor i (the encode is bound by instruction issue,
- * the amax pass by HBM reads), so a list costs about one amax pass plus n
- * encodes.  Other configurations run the entries one after another.
+ * pipelined: the launch that encodes tensor i also runs the amax pass of
+ * tensor i+1 (every warp loads its next-tensor segment before encoding and
+ * folds it into its max afterwards; the encode is bound by instruction
+ * issue, the amax pass by HBM reads), so a list costs about one amax pass
+ * plus n encodes.  Other configurations run the entries one after another.
  * Host arrays must hold n entries; errors as for fos_quantize (the first
  * failing entry's status, nothing launched).
  */
