@@ -305,11 +305,15 @@ __device__ __forceinline__ void build_table(float2* tbl, float S, int lane) {
     __syncwarp();
 }
 
-// One entry of the common-scale table (see build_table).
-__device__ __forceinline__ float2 table_entry(float S, int c) {
+// The common-scale table filled by a whole CTA of kThreads = 256 threads,
+// one division each: thread t < 128 writes r of code t, thread 128 + t
+// writes d of code t.
+__device__ __forceinline__ void fill_table_cta(float2* tbl, float S, int tid) {
+    const int c = tid & 127;
     const float sig = e4m3_f32((uint32_t)c);
-    if (sig == 0.0f) return make_float2(0.0f, 0.0f);
-    return make_float2(fdiv(S, sig), fdiv(sig, S));
+    float v = 0.0f;
+    if (sig != 0.0f) v = (tid < 128) ? fdiv(S, sig) : fdiv(sig, S);
+    reinterpret_cast<float*>(tbl)[2 * c + (tid >> 7)] = v;
 }
 
 __device__ __forceinline__ uint32_t pack4(uint32_t b0, uint32_t b1, uint32_t b2, uint32_t b3) {

@@ -237,16 +237,18 @@ __global__ void __launch_bounds__(kThreads, min_ctas<EM>()) k_quant1x16(const En
 // 1x16 quantize with a per-row scale in one pass: one CTA per row at a time
 // (grid-stride over rows).  Each thread keeps its K blocks of the row in
 // registers; the row amax (when it is not given) is a CTA max-reduction and
-// is written out, the CTA builds the row's common-scale table, then encodes.
-// The next row is loaded before the current one is encoded.  Two barriers per
-// row: shared buffers are rewritten only after every thread passed the next
-// row's first barrier, i.e. finished reading them.
+// is written out, the CTA builds the row's common-scale table (one division
+// per thread), then encodes.  The next row is loaded before the current one
+// is encoded.  The table is double-buffered by row parity: a buffer is
+// rewritten two rows later, after every thread has passed the barrier of the
+// row in between and so finished reading it.  One barrier per row (table
+// ready) with the amax given, two with the amax computed (reduction, table).
 // ------------------------------------------------------------------------
 template <In IT, Err EM, int K>
 __global__ void __launch_bounds__(kThreads) k_quant1x16_rowpass(const EncArgs a) {
     chain_wait();
     chain_release();
-    __shared__ float2 s_tbl[128];
+    __shared__ float2 s_tbl[2][128];
     __shared__ float s_red[kWarps];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint64_t nz = pk(a.neg_zero, a.neg_zero);
@@ -262,7 +264,8 @@ __global__ void __launch_bounds__(kThreads) k_quant1x16_rowpass(const EncArgs a)
         load_if<IT, kEncHint>(cur[k], xb + (row * a.nb + j) * kBytes, j < a.nb);
     }
     uint32_t dummy[8];
-    for (; row < a.rows; row += gridDim.x) {
+    int par = 0;
+    for (; row < a.rows; row += gridDim.x, par ^= 1) {
         const int64_t rown = row + gridDim.x;
 #pragma unroll
         for (int k = 0; k < K; ++k) {
@@ -282,7 +285,6 @@ __global__ void __launch_bounds__(kThreads) k_quant1x16_rowpass(const EncArgs a)
         float A;
         if (a.amax_given) {
             A = a.amax[row];
-            __syncthreads();
         } else {
             m = warp_max_dev(m);
             if (lane == 0) s_red[warp] = m;
@@ -293,7 +295,7 @@ __global__ void __launch_bounds__(kThreads) k_quant1x16_rowpass(const EncArgs a)
             if (tid == 0) amax_out[row] = A;
         }
         const float S = global_scale(A, a.six_bound);
-        if (tid < 128) s_tbl[tid] = table_entry(S, tid);
+        fill_table_cta(s_tbl[par], S, tid);
         __syncthreads();
 #pragma unroll
         for (int k = 0; k < K; ++k) {
@@ -302,7 +304,7 @@ __global__ void __launch_bounds__(kThreads) k_quant1x16_rowpass(const EncArgs a)
                 uint64_t xp[8];
                 widen<IT>(cur[k], xp);
                 uint32_t code[2], scale;
-                encode_block_amax<EM, Out::NONE>(xp, bam[k], S, s_tbl, nz, code, scale, dummy);
+                encode_block_amax<EM, Out::NONE>(xp, bam[k], S, s_tbl[par], nz, code, scale, dummy);
                 const int64_t b = row * a.nb + j;
                 st64(a.codes + b * 8, code[0], code[1]);
                 st8(a.scales + b, scale);
