@@ -11,13 +11,13 @@ the L2, so every pass reads its input from HBM.
 once per tensor (read 2 B + write 0.5 B codes + 1/16 B scale per element);
 the amax pass's second read of x is not counted, so the figure is strict.
 The step is the pipelined list quantize (fos_quantize_list's launches): the
-amax pass of tensor 0, then one launch per tensor that encodes it while
-other warps run the amax pass of the next tensor.  `roofline` is that
-overlapped launch (timed in its own loop of the three stages; its
-algorithmic bytes are the encode's plus the next tensor's read).  `e2e`
-repeats the step through the same C-ABI calls starting from
-pinned host buffers, with the host->device copy of the inputs and the
-device->host copy of codes and scales inside the timed region.
+amax pass of tensor 0, then one launch per tensor that encodes it and runs
+the amax pass of the next tensor.  `roofline` is that overlapped launch
+(timed in its own loop of the three stages; its algorithmic bytes are the
+encode's plus the next tensor's read).  `e2e` repeats the step through the
+same C-ABI calls starting from pinned host buffers, with the host->device
+copy of the inputs and the device->host copy of codes and scales inside the
+timed region, the copies on their own streams overlapping the encodes.
 
 --impl reference times the CPU oracle (the reference for this path) on a
 bounded sample of the same workload.
@@ -355,9 +355,13 @@ def run_fos(args):
 
 
 def _e2e(fos, xs, cfg, stream, args, ws, dev):
-    """The step from pinned host buffers through the public API: H2D of the
-    four inputs, amax + encode (fos_quantize computes the amax), D2H of codes
-    and scales, all inside the timed region."""
+    """The step from pinned host buffers through the public API, with the
+    host->device copy of the four inputs and the device->host copy of codes
+    and scales inside the timed region.  The copies run on their own streams
+    and overlap the quantization: tensor i is encoded (fos_quantize_overlap,
+    which also runs the amax pass of tensor i+1) as soon as tensors i and i+1
+    have arrived, and its codes go back while later tensors are still being
+    copied in.  The host link, not the GPU, bounds this number."""
     import torch
     dev = xs[0].device
     hx = [x.cpu().pin_memory() for x in xs]
@@ -367,14 +371,34 @@ def _e2e(fos, xs, cfg, stream, args, ws, dev):
     ds = [torch.empty(ROWS, COLS // 16, dtype=torch.uint8, device=dev) for _ in xs]
     hc = [torch.empty(ROWS, COLS // 2, dtype=torch.uint8).pin_memory() for _ in xs]
     hs = [torch.empty(ROWS, COLS // 16, dtype=torch.uint8).pin_memory() for _ in xs]
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    e_start = torch.cuda.Event()
+    e_in = [torch.cuda.Event() for _ in xs]
+    e_out = [torch.cuda.Event() for _ in xs]
 
     def step():
-        for i in range(4):
-            dx[i].copy_(hx[i], non_blocking=True)
-        fos.quantize_list(dx, cfg, amaxes=am, codes=dc, scales=ds, amax_given=False)
-        for i in range(4):
-            hc[i].copy_(dc[i], non_blocking=True)
-            hs[i].copy_(ds[i], non_blocking=True)
+        main = torch.cuda.current_stream(dev)
+        e_start.record(main)  # the previous step (results on the host) is done
+        s_in.wait_event(e_start)
+        s_out.wait_event(e_start)
+        with torch.cuda.stream(s_in):
+            for i in range(4):
+                dx[i].copy_(hx[i], non_blocking=True)
+                e_in[i].record(s_in)
+        main.wait_event(e_in[0])
+        fos.amax(dx[0], out=am[0])
+        for i in range(3):
+            main.wait_event(e_in[i + 1])
+            fos.quantize_overlap(dx[i], am[i], dc[i], ds[i], dx[i + 1], am[i + 1], cfg)
+            e_out[i].record(main)
+        fos.quantize(dx[3], cfg, amax=am[3], codes=dc[3], scales=ds[3])
+        e_out[3].record(main)
+        with torch.cuda.stream(s_out):
+            for i in range(4):
+                s_out.wait_event(e_out[i])
+                hc[i].copy_(dc[i], non_blocking=True)
+                hs[i].copy_(ds[i], non_blocking=True)
+        main.wait_stream(s_out)
 
     reps = max(3, args.steps // 10)
     for _ in range(3):
