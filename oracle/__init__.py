@@ -45,7 +45,8 @@ def use_library(path):
 class OrcConfig(ctypes.Structure):
     _fields_ = [("block16x16", ctypes.c_int), ("four_over_six", ctypes.c_int),
                 ("mse", ctypes.c_int), ("err_f16", ctypes.c_int), ("bound", ctypes.c_int),
-                ("row_scaled", ctypes.c_int), ("amax_is_input", ctypes.c_int)]
+                ("row_scaled", ctypes.c_int), ("amax_is_input", ctypes.c_int),
+                ("seq_order", ctypes.c_int)]
 
 
 OUT_F32, OUT_BF16, OUT_F16 = 0, 1, 2
@@ -87,7 +88,9 @@ def _declare(L):
 @dataclass
 class Config:
     """Knobs of the method: block shape, standard vs four-over-six, error
-    metric and precision, E4M3 bound, scale granularity."""
+    metric and precision, E4M3 bound, scale granularity, and the order in
+    which a block's 16 error terms are summed (pinned tree, or sequential
+    with seq_order, 1x16 only)."""
     block16x16: bool = False
     four_over_six: bool = True
     mse: bool = True
@@ -95,11 +98,12 @@ class Config:
     bound: int = 448
     row_scaled: bool = False
     amax_is_input: bool = False
+    seq_order: bool = False
 
     def c(self):
         return OrcConfig(int(self.block16x16), int(self.four_over_six), int(self.mse),
                          int(self.err_f16), int(self.bound), int(self.row_scaled),
-                         int(self.amax_is_input))
+                         int(self.amax_is_input), int(self.seq_order))
 
 
 def _ptr(a):

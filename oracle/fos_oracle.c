@@ -50,6 +50,7 @@ typedef struct {
     int bound;          /* E4M3 bound used in the global scale: 448 or 256   */
     int row_scaled;     /* 0: per-tensor amax, 1: per-row amax               */
     int amax_is_input;  /* 1: amax given, 0: oracle computes and writes it   */
+    int seq_order;      /* 0: pinned tree reduction, 1: sequential (R16)     */
 } orc_config;
 
 enum { ORC_OK = 0, ORC_BAD = 1 };
@@ -215,6 +216,18 @@ static float tree16(const float* in)
     return t[0];
 }
 
+/* Sequential accumulation of the 16 terms in element order (R16): the
+ * Transformer Engine term order the Megatron PR keeps for its sequential
+ * error accumulation ("Packed pair arithmetic"): acc = t[0], then
+ * acc = acc + t[i] for i = 1..15 (starting from +0 gives the same sums, the
+ * terms being >= +0). */
+static float seq16(const float* in)
+{
+    float acc = in[0];
+    for (int i = 1; i < 16; ++i) acc = acc + in[i];
+    return acc;
+}
+
 typedef struct {
     uint32_t sc_code;  /* E4M3 bits of the block scale          */
     float sigma;       /* its exact decode                      */
@@ -252,7 +265,7 @@ static void candidate(const float* x, int nrows, int64_t ld, float a_b, float S,
             float e = xi - deq;
             terms[i] = cfg->mse ? e * e : fabsf(e);
         }
-        P[rr] = tree16(terms);
+        P[rr] = cfg->seq_order ? seq16(terms) : tree16(terms);
     }
     c->err = (nrows == 1) ? P[0] : tree16(P);        /* R8 */
 }
@@ -383,6 +396,7 @@ static int check_shape(int64_t rows, int64_t cols, const orc_config* cfg)
     if (rows < 0 || cols < 0 || cols % 16 != 0) return ORC_BAD;
     if (cfg->block16x16 && rows % 16 != 0) return ORC_BAD;
     if (cfg->bound != 448 && cfg->bound != 256) return ORC_BAD;
+    if (cfg->seq_order && cfg->block16x16) return ORC_BAD; /* R16: 1x16 only */
     return ORC_OK;
 }
 

@@ -61,6 +61,27 @@ class Inexact(Exception):
 def candidate(rows, S: F, k: int, mse: bool, f16: bool):
     """rows: list of lists of 16 Fractions.  Returns dict with codes (list of
     lists of 4-bit codes), sc (E4M3 code), err (Fraction), ambiguous (bool)."""
+    c = candidate_terms(rows, S, k, mse, f16)
+    partials = c.pop("terms")
+    # Every partial sum of the nonnegative dyadic terms is a multiple of the
+    # finest grain and at most the total; below 2^24 grains all are exact in
+    # binary32, so the reduction order cannot matter for these blocks.
+    allterms = [t for ts in partials for t in ts]
+    grain = max((t.denominator for t in allterms), default=1)
+    if grain & (grain - 1):
+        raise Inexact("non-dyadic term")
+    total = sum(allterms, F(0))
+    if total * grain >= 2**24:
+        raise Inexact("error sum not exact")
+    c["err"] = total
+    return c
+
+
+def candidate_terms(rows, S: F, k: int, mse: bool, f16: bool):
+    """Like candidate() but stops before the reduction: returns codes, sc,
+    ambiguous and terms (per row, the 16 exact error terms, each exactly a
+    binary32 value), for blocks whose per-element arithmetic is exact even
+    when their sum is not."""
     a_b = max(abs(v) for r in rows for v in r)
     t = a_b * S
     s = t / k
@@ -97,17 +118,7 @@ def candidate(rows, S: F, k: int, mse: bool, f16: bool):
             terms.append(term)
         codes.append(crow)
         partials.append(terms)
-    # Every partial sum of the nonnegative dyadic terms is a multiple of the
-    # finest grain and at most the total; below 2^24 grains all are exact in
-    # binary32, so the reduction order cannot matter for these blocks.
-    allterms = [t for ts in partials for t in ts]
-    grain = max((t.denominator for t in allterms), default=1)
-    if grain & (grain - 1):
-        raise Inexact("non-dyadic term")
-    total = sum(allterms, F(0))
-    if total * grain >= 2**24:
-        raise Inexact("error sum not exact")
-    return {"codes": codes, "sc": sc, "err": total, "ambiguous": ambiguous}
+    return {"codes": codes, "sc": sc, "terms": partials, "ambiguous": ambiguous}
 
 
 def block(rows, S: F, four_over_six=True, mse=True, f16=False):

@@ -68,6 +68,91 @@ def test_tree_order_golden(orc):
     assert struct.pack(">f", float(e6[0, 0])).hex().upper() == bits_hex
 
 
+def test_seq_order_golden(orc):
+    (bits_hex,) = _numbers("seq_order.txt")[0]
+    x = np.full((1, 16), np.float32(0.5) + np.float32(2.0 ** -24), np.float32)
+    x[0, 0] = 5.0
+    x[0, 15] = 6.0
+    cfg = orc.Config(four_over_six=True, mse=False, err_f16=False, amax_is_input=True,
+                     seq_order=True)
+    _, _, _, e6, _ = orc.quantize(x, cfg, amax=[2688.0], with_errors=True)
+    assert struct.pack(">f", float(e6[0, 0])).hex().upper() == bits_hex
+
+
+def _fold_seq(terms):
+    acc = np.float32(float(terms[0]))
+    for t in terms[1:]:
+        acc = np.float32(acc + np.float32(float(t)))
+    return acc
+
+
+def _fold_tree(terms):
+    t = [np.float32(float(v)) for v in terms]
+    w = 8
+    while w >= 1:
+        for i in range(w):
+            t[i] = np.float32(t[i] + t[i + w])
+        w //= 2
+    return t[0]
+
+
+@pytest.mark.parametrize("mse", [False, True])
+def test_seq_order_against_binary32_folds(orc, mse):
+    """Blocks whose element errors are exact but whose sums are not: the
+    exact-rational model gives the 16 terms; numpy binary32 additions fold
+    them in element order (and, as a control, in the pinned tree order).  The
+    oracle's sequential-order errors, codes and scales must follow the
+    sequential fold."""
+    rng = np.random.default_rng(53 + mse)
+    grid = [F(1, 2), F(1), F(3, 2), F(2), F(3), F(4)]
+    rows, want = [], []
+    differs = 0
+    for _ in range(4000):
+        if len(rows) == 64:
+            break
+        row = []
+        for _ in range(16):
+            g = grid[int(rng.integers(len(grid)))]
+            if mse:  # errors of at most 12 significant bits, so that e*e is exact
+                step = F(1, 2 ** 13)
+            else:    # errors down to one unit in the last place of x
+                step = F(2) ** (int(np.floor(np.log2(float(g)))) - 23)
+            v = g + int(rng.integers(-40, 41)) * step * 2 ** int(rng.integers(0, 6))
+            row.append(-v if rng.random() < 0.5 else v)
+        # one element on a grid midpoint (a large error term next to the small
+        # ones, so that sums need more than 24 bits) and the block amax 6
+        i5, i6 = rng.choice(16, 2, replace=False)
+        row[int(i5)] = F(5) if rng.random() < 0.5 else F(-5)
+        row[int(i6)] = F(6)
+        try:
+            c6 = em.candidate_terms([row], F(1), 6, mse, False)
+            c4 = em.candidate_terms([row], F(1), 4, mse, False)
+        except em.Inexact:
+            continue
+        if c6["ambiguous"] or c4["ambiguous"]:
+            continue
+        e6, e4 = _fold_seq(c6["terms"][0]), _fold_seq(c4["terms"][0])
+        differs += int(e6 != _fold_tree(c6["terms"][0]) or e4 != _fold_tree(c4["terms"][0]))
+        sel = c4 if e4 < e6 else c6
+        rows.append(row)
+        want.append((e6, e4, sel))
+    assert len(rows) == 64
+    assert differs >= 8  # the draw really separates the two orders
+    x = np.array([[float(v) for v in r] for r in rows], np.float32)
+    cfg = orc.Config(four_over_six=True, mse=mse, amax_is_input=True, seq_order=True)
+    codes, scales, _, e6, e4 = orc.quantize(x, cfg, amax=[2688.0], with_errors=True)
+    for i, (w6, w4, sel) in enumerate(want):
+        assert e6[i, 0] == w6 and e4[i, 0] == w4, i
+        assert bytes(codes[i]) == em.pack_row(sel["codes"][0]), i
+        assert scales[i, 0] == sel["sc"], i
+
+
+def test_seq_order_rejects_16x16(orc):
+    x = np.zeros((16, 16), np.float32)
+    with pytest.raises(ValueError):
+        orc.quantize(x, orc.Config(block16x16=True, seq_order=True))
+
+
 # ------------------------------------------------------- exact-rational model
 NICE_SIGMA = [F(1), F(9, 8), F(5, 4), F(11, 8), F(3, 2), F(13, 8), F(7, 4), F(15, 8)]
 

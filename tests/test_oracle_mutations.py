@@ -15,6 +15,10 @@ MUTANTS = {
     "tree_sequential": ("for (int w = 8; w >= 1; w /= 2)\n        for (int i = 0; i < w; ++i) "
                         "t[i] = t[i] + t[i + w];\n    return t[0];",
                         "float s = 0.0f; for (int i = 0; i < 16; ++i) s = s + t[i];\n    return s;"),
+    "seq_as_tree": ("P[rr] = cfg->seq_order ? seq16(terms) : tree16(terms);",
+                    "P[rr] = tree16(terms);"),
+    "seq_reversed": ("float acc = in[0];\n    for (int i = 1; i < 16; ++i) acc = acc + in[i];",
+                     "float acc = in[15];\n    for (int i = 14; i >= 0; --i) acc = acc + in[i];"),
     "swap_r_d": ("c->r = S / c->sigma;\n        c->d = c->sigma / S;",
                  "c->r = c->sigma / S;\n        c->d = S / c->sigma;"),
     "select_on_tie": ("return (c4->err < c6->err) ? c4 : c6;",
