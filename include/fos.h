@@ -68,6 +68,7 @@ enum { FOS_MODE_STANDARD = 0, FOS_MODE_4OVER6 = 1 };
 enum { FOS_MAE = 0, FOS_MSE = 1 };
 enum { FOS_ERR_EXACT_F32 = 0, FOS_ERR_F16 = 1 };
 enum { FOS_SCALE_TENSOR = 0, FOS_SCALE_ROW = 1 };
+enum { FOS_ORDER_TREE = 0, FOS_ORDER_SEQ = 1 };
 
 /* The knobs the pages name (Megatron PR "Fuse NVFP4 fake-QAT quantize-
  * dequantize with CuTe DSL", numerical contract: standard NVFP4 plus 4over6
@@ -81,6 +82,13 @@ typedef struct {
     int e4m3_bound;    /* 448 | 256: E4M3 value the global scale maps the amax to */
     int granularity;   /* FOS_SCALE_TENSOR | FOS_SCALE_ROW                       */
     int amax_is_input; /* 1: caller supplies amax; 0: library computes, writes it */
+    int err_order;     /* how a block's 16 error terms are summed (4over6 only):
+                        * FOS_ORDER_TREE (0): the pinned width-16 tree of the
+                        *   torchao fast-path PR, for w = 8,4,2,1: t[i] += t[i+w];
+                        * FOS_ORDER_SEQ (1): in element order, t0 + t1 + ... + t15
+                        *   (the Transformer Engine term order the Megatron PR
+                        *   keeps, "Packed pair arithmetic"); 1x16 blocks only,
+                        *   FOS_ERR_UNSUPPORTED with 16x16 in 4over6 mode.     */
 } fos_config;
 
 /*

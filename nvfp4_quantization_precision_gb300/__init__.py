@@ -43,7 +43,8 @@ class FosError(RuntimeError):
 class FosConfig(ctypes.Structure):
     _fields_ = [("block", ctypes.c_int), ("mode", ctypes.c_int), ("err_metric", ctypes.c_int),
                 ("err_precision", ctypes.c_int), ("e4m3_bound", ctypes.c_int),
-                ("granularity", ctypes.c_int), ("amax_is_input", ctypes.c_int)]
+                ("granularity", ctypes.c_int), ("amax_is_input", ctypes.c_int),
+                ("err_order", ctypes.c_int)]
 
 
 @dataclass(frozen=True)
@@ -55,11 +56,12 @@ class Config:
     err_f16: bool = False
     bound: int = 448
     row_scaled: bool = False
+    seq_order: bool = False  # sum a block's error terms in element order (1x16 only)
 
     def c(self, amax_is_input):
         return FosConfig(int(self.block16x16), int(self.four_over_six), int(self.mse),
                          int(self.err_f16), int(self.bound), int(self.row_scaled),
-                         int(bool(amax_is_input)))
+                         int(bool(amax_is_input)), int(self.seq_order))
 
 
 _lib = None

@@ -32,13 +32,28 @@ fos_status check_config(const fos_config* cfg) {
     if (cfg->granularity != FOS_SCALE_TENSOR && cfg->granularity != FOS_SCALE_ROW)
         return FOS_ERR_INVALID_ARG;
     if (cfg->amax_is_input != 0 && cfg->amax_is_input != 1) return FOS_ERR_INVALID_ARG;
+    if (cfg->err_order != FOS_ORDER_TREE && cfg->err_order != FOS_ORDER_SEQ)
+        return FOS_ERR_INVALID_ARG;
     if (cfg->e4m3_bound != 448 && cfg->e4m3_bound != 256) return FOS_ERR_UNSUPPORTED;
+    return FOS_OK;
+}
+
+// The sequential term order is offered for 1x16 blocks (its source is a 1x16
+// path); standard mode has no candidate errors, so the knob is moot there.
+fos_status check_order(const fos_config* cfg) {
+    if (cfg->err_order == FOS_ORDER_SEQ && cfg->block == FOS_BLOCK_16X16 &&
+        cfg->mode == FOS_MODE_4OVER6)
+        return FOS_ERR_UNSUPPORTED;
     return FOS_OK;
 }
 
 Err err_of(const fos_config* cfg) {
     if (cfg->mode == FOS_MODE_STANDARD) return Err::STD;
     const bool mse = cfg->err_metric == FOS_MSE, h = cfg->err_precision == FOS_ERR_F16;
+    if (cfg->err_order == FOS_ORDER_SEQ) {
+        if (mse) return h ? Err::MSE_HS : Err::MSE_S;
+        return h ? Err::MAE_HS : Err::MAE_S;
+    }
     if (mse) return h ? Err::MSE_H : Err::MSE;
     return h ? Err::MAE_H : Err::MAE;
 }
@@ -279,6 +294,8 @@ fos_status check_quant_args(const void* x, int64_t rows, int64_t cols, const fos
                             const float* amax, const uint8_t* codes, const uint8_t* scales) {
     fos_status st = check_shape(rows, cols, cfg->block == FOS_BLOCK_16X16);
     if (st) return st;
+    st = check_order(cfg);
+    if (st) return st;
     if (rows == 0 || cols == 0) {
         if (!cfg->amax_is_input && !(cfg->granularity == FOS_SCALE_ROW && rows == 0) && !amax)
             return FOS_ERR_INVALID_ARG;
@@ -465,6 +482,8 @@ fos_status fos_quantize_grouped(const void* x, fos_dtype dt, int64_t rows, int64
     fos_status st = check_config(cfg);
     if (st) return st;
     st = check_shape(rows, cols, cfg->block == FOS_BLOCK_16X16);
+    if (st) return st;
+    st = check_order(cfg);
     if (st) return st;
     if (G < 1) return FOS_ERR_INVALID_ARG;
     if (G > FOS_GROUPED_MAX_GROUPS) return FOS_ERR_UNSUPPORTED;

@@ -23,16 +23,26 @@ namespace fos {
 
 enum class In : int { BF16 = 0, F16 = 1, F32 = 2 };
 // STD: standard NVFP4 (map-to-6 only).  The others are four-over-six with the
-// given candidate-error metric; *_H compares candidates decoded to FP16.
-enum class Err : int { STD = 0, MAE = 1, MSE = 2, MAE_H = 3, MSE_H = 4 };
+// given candidate-error metric; *_H compares candidates decoded to FP16; *_S
+// sums a block's error terms in element order instead of the pinned tree.
+enum class Err : int {
+    STD = 0, MAE = 1, MSE = 2, MAE_H = 3, MSE_H = 4, MAE_S = 5, MSE_S = 6, MAE_HS = 7, MSE_HS = 8
+};
 enum class Src : int { TENSOR = 0, ROW = 1, GROUP = 2 };
 
 constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
 constexpr float kFltMax = 3.402823466e38f;
 
-__host__ __device__ constexpr bool err_is_mse(Err e) { return e == Err::MSE || e == Err::MSE_H; }
-__host__ __device__ constexpr bool err_is_f16(Err e) { return e == Err::MAE_H || e == Err::MSE_H; }
+__host__ __device__ constexpr bool err_is_mse(Err e) {
+    return e == Err::MSE || e == Err::MSE_H || e == Err::MSE_S || e == Err::MSE_HS;
+}
+__host__ __device__ constexpr bool err_is_f16(Err e) {
+    return e == Err::MAE_H || e == Err::MSE_H || e == Err::MAE_HS || e == Err::MSE_HS;
+}
+__host__ __device__ constexpr bool err_is_seq(Err e) {
+    return e == Err::MAE_S || e == Err::MSE_S || e == Err::MAE_HS || e == Err::MSE_HS;
+}
 template <In IT> struct InTraits;
 template <> struct InTraits<In::BF16> { static constexpr int kWords = 8; };   // 16 x 2 B
 template <> struct InTraits<In::F16> { static constexpr int kWords = 8; };
@@ -381,6 +391,21 @@ __device__ __forceinline__ float candidate(const uint64_t (&xp)[8], float r, flo
     }
     if constexpr (EM == Err::STD) {
         return 0.0f;
+    } else if constexpr (err_is_seq(EM)) {
+        // element order: ((t0 + t1) + t2) + ... + t15
+        float acc = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            float lo, hi;
+            upk(term[j], lo, hi);
+            if constexpr (!err_is_mse(EM)) {
+                lo = fabsf(lo);
+                hi = fabsf(hi);
+            }
+            acc = (j == 0) ? lo : fadd(acc, lo);
+            acc = fadd(acc, hi);
+        }
+        return acc;
     } else {
         uint64_t t0, t1, t2, t3;
         if constexpr (err_is_mse(EM)) {

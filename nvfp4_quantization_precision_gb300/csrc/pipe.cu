@@ -14,6 +14,10 @@ static cudaError_t by_err(Err em, const PipeArgs& a, cudaStream_t s) {
         case Err::MSE: return launch_persistent(k_quant1x16_pipe<IT, Err::MSE>, a, units, 0, s);
         case Err::MAE_H: return launch_persistent(k_quant1x16_pipe<IT, Err::MAE_H>, a, units, 0, s);
         case Err::MSE_H: return launch_persistent(k_quant1x16_pipe<IT, Err::MSE_H>, a, units, 0, s);
+        case Err::MAE_S: return launch_persistent(k_quant1x16_pipe<IT, Err::MAE_S>, a, units, 0, s);
+        case Err::MSE_S: return launch_persistent(k_quant1x16_pipe<IT, Err::MSE_S>, a, units, 0, s);
+        case Err::MAE_HS: return launch_persistent(k_quant1x16_pipe<IT, Err::MAE_HS>, a, units, 0, s);
+        case Err::MSE_HS: return launch_persistent(k_quant1x16_pipe<IT, Err::MSE_HS>, a, units, 0, s);
     }
     return cudaErrorInvalidValue;
 }

@@ -11,6 +11,10 @@ static cudaError_t by_err(Err em, const QdqArgs& a, cudaStream_t s) {
         case Err::MSE: return launch_persistent(k_qdq1x16<IT, Err::MSE>, a, a.units, 0, s);
         case Err::MAE_H: return launch_persistent(k_qdq1x16<IT, Err::MAE_H>, a, a.units, 0, s);
         case Err::MSE_H: return launch_persistent(k_qdq1x16<IT, Err::MSE_H>, a, a.units, 0, s);
+        case Err::MAE_S: return launch_persistent(k_qdq1x16<IT, Err::MAE_S>, a, a.units, 0, s);
+        case Err::MSE_S: return launch_persistent(k_qdq1x16<IT, Err::MSE_S>, a, a.units, 0, s);
+        case Err::MAE_HS: return launch_persistent(k_qdq1x16<IT, Err::MAE_HS>, a, a.units, 0, s);
+        case Err::MSE_HS: return launch_persistent(k_qdq1x16<IT, Err::MSE_HS>, a, a.units, 0, s);
     }
     return cudaErrorInvalidValue;
 }

@@ -30,6 +30,10 @@ cudaError_t launch_quant1x16_f32(Err em, Src src, const EncArgs& a, cudaStream_t
         case Err::MSE: return by_src<Err::MSE>(src, a, s);
         case Err::MAE_H: return by_src<Err::MAE_H>(src, a, s);
         case Err::MSE_H: return by_src<Err::MSE_H>(src, a, s);
+        case Err::MAE_S: return by_src<Err::MAE_S>(src, a, s);
+        case Err::MSE_S: return by_src<Err::MSE_S>(src, a, s);
+        case Err::MAE_HS: return by_src<Err::MAE_HS>(src, a, s);
+        case Err::MSE_HS: return by_src<Err::MSE_HS>(src, a, s);
     }
     return cudaErrorInvalidValue;
 }
@@ -50,6 +54,10 @@ cudaError_t launch_quant1x16_rowpass_f32(Err em, int k, const EncArgs& a, cudaSt
         case Err::MSE: return rowpass<Err::MSE>(k, a, s);
         case Err::MAE_H: return rowpass<Err::MAE_H>(k, a, s);
         case Err::MSE_H: return rowpass<Err::MSE_H>(k, a, s);
+        case Err::MAE_S: return rowpass<Err::MAE_S>(k, a, s);
+        case Err::MSE_S: return rowpass<Err::MSE_S>(k, a, s);
+        case Err::MAE_HS: return rowpass<Err::MAE_HS>(k, a, s);
+        case Err::MSE_HS: return rowpass<Err::MSE_HS>(k, a, s);
     }
     return cudaErrorInvalidValue;
 }

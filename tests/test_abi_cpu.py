@@ -68,6 +68,8 @@ FAKE = ctypes.c_void_p(0x10000)  # never dereferenced: every call below fails va
     (dict(granularity=2), fos.FOS_ERR_INVALID_ARG),
     (dict(amax_is_input=5), fos.FOS_ERR_INVALID_ARG),
     (dict(e4m3_bound=300), fos.FOS_ERR_UNSUPPORTED),
+    (dict(err_order=2), fos.FOS_ERR_INVALID_ARG),
+    (dict(block=1, err_order=1), fos.FOS_ERR_UNSUPPORTED),  # sequential order: 1x16 only
 ])
 def test_quantize_rejects_bad_config(L, kw, rc):
     c = _cfg(**kw)

@@ -33,12 +33,12 @@ def _built():
         pytest.skip("no CUDA device")
 
 
-def _cfgs(mode, bound=448, row=False, b16=False):
+def _cfgs(mode, bound=448, row=False, b16=False, seq=False):
     f, m, h = MODES[mode]
     return (fos.Config(block16x16=b16, four_over_six=f, mse=m, err_f16=h, bound=bound,
-                       row_scaled=row),
+                       row_scaled=row, seq_order=seq),
             oracle.Config(block16x16=b16, four_over_six=f, mse=m, err_f16=h, bound=bound,
-                          row_scaled=row))
+                          row_scaled=row, seq_order=seq))
 
 
 def _u16(t):
@@ -506,3 +506,81 @@ def test_quantize_overlap_stage(mode):
     oc, os_, _ = oracle.quantize(xf, ocfg2, amax=a.cpu().numpy())
     assert np.array_equal(c.cpu().numpy(), oc) and np.array_equal(s_.cpu().numpy(), os_)
     assert np.array_equal(_u32(an), oracle.amax_tensor(xnf).view(np.uint32))
+
+
+# ------------------------------------------------------------------ sequential term order
+SEQ_MODES = ["mae", "mse", "mae_f16", "mse_f16"]
+
+
+@pytest.mark.parametrize("dt", ["bf16", "f16", "f32"])
+@pytest.mark.parametrize("mode", SEQ_MODES)
+@pytest.mark.parametrize("row", [False, True])
+def test_quantize_1x16_seq_order(dt, mode, row):
+    """Error terms summed in element order (the Transformer Engine order):
+    per-tensor and per-row scale (the one-pass row kernel for the 4096-column
+    case), amax computed and given, all four families."""
+    gcfg, ocfg = _cfgs(mode, 448, row, seq=True)
+    for i, (shape, fam) in enumerate(zip([(33, 4096), (70, 528), (5, 2048), (128, 1040)],
+                                         workloads.FAMILIES)):
+        _check_quant(_x(*shape, fam, seed=40 + i, dt=dt), gcfg, ocfg, amax_given=(i % 2 == 1))
+
+
+def test_seq_order_changes_choices_on_gpu():
+    """On this input the two orders select differently in some blocks (the
+    oracle gives 8 differing scale bytes for MAE), so the sequential tests
+    are not satisfied by the tree order by accident."""
+    x = _x(256, 4096, "F2", 7, "bf16")
+    a = torch.from_numpy(oracle.amax_tensor(x.float().numpy())).to(DEV)
+    ct, st, _ = fos.quantize(x.to(DEV), fos.Config(mse=False), amax=a)
+    cs, ss, _ = fos.quantize(x.to(DEV), fos.Config(mse=False, seq_order=True), amax=a)
+    torch.cuda.synchronize()
+    assert not torch.equal(ss, st)
+
+
+@pytest.mark.parametrize("dt", ["bf16", "f16"])
+@pytest.mark.parametrize("mode", SEQ_MODES)
+def test_qdq_list_seq_order(dt, mode):
+    gcfg, ocfg = _cfgs(mode, 256, seq=True)
+    shapes = [(64, 1024), (7, 1040), (48, 272), (1, 16)]
+    xs = [workloads.qdq_weights(1, r, c, seed=60 + i, dtype=DTYPES[dt])[0]
+          for i, (r, c) in enumerate(shapes)]
+    outs = fos.qdq([x.to(DEV) for x in xs], gcfg)
+    torch.cuda.synchronize()
+    for x, o in zip(xs, outs):
+        ref, _ = oracle.qdq(x.float().numpy(), ocfg, dt)
+        assert np.array_equal(_u16(o), ref)
+
+
+@pytest.mark.parametrize("mode", SEQ_MODES)
+def test_quantize_list_seq_order(mode):
+    """The pipelined list launches (encode of tensor i with the amax pass of
+    tensor i+1) with the sequential order."""
+    gcfg, ocfg = _cfgs(mode, 448, seq=True)
+    xs = [_x(r, c, fam, 80 + i, "bf16") for i, ((r, c), fam) in
+          enumerate(zip([(64, 1024), (7, 1040), (256, 2048)], workloads.FAMILIES))]
+    gc, gs, ga = fos.quantize_list([x.to(DEV) for x in xs], gcfg)
+    torch.cuda.synchronize()
+    for x, c, s_, a in zip(xs, gc, gs, ga):
+        oc, os_, oa = oracle.quantize(x.float().numpy(), ocfg)
+        assert np.array_equal(_u32(a), oa.view(np.uint32))
+        assert np.array_equal(s_.cpu().numpy(), os_) and np.array_equal(c.cpu().numpy(), oc)
+
+
+def test_grouped_seq_order():
+    R, C = 512, 272
+    offs = workloads.moe_offsets(R, 12, seed=5, n_empty=3)
+    x = workloads.moe_activations(R, C, offs, seed=6)
+    gcfg, ocfg = _cfgs("mse_f16", 448, seq=True)
+    oc, os_, oa = oracle.quantize_grouped(x.float().numpy(), offs.numpy(), ocfg)
+    gc, gs, ga = fos.quantize_grouped(x.to(DEV), offs.to(DEV), gcfg)
+    torch.cuda.synchronize()
+    assert np.array_equal(_u32(ga), oa.view(np.uint32))
+    assert np.array_equal(gc.cpu().numpy(), oc) and np.array_equal(gs.cpu().numpy(), os_)
+
+
+def test_seq_order_with_16x16_is_unsupported():
+    x = torch.zeros(16, 16, dtype=torch.bfloat16, device=DEV)
+    with pytest.raises(fos.FosError):
+        fos.quantize(x, fos.Config(block16x16=True, seq_order=True))
+    # standard mode has no candidate errors, so the order is moot and accepted
+    fos.quantize(x, fos.Config(block16x16=True, four_over_six=False, seq_order=True))
