@@ -450,6 +450,12 @@ def _rows(fos, xs, stream, peak):
         name = ("std" if not four else ("mse" if mse else "mae") + ("_f16" if f16 else "_exact")
                 ) + "_%d_%s" % (bound, "row" if row else "tensor")
         sweep[name] = round(ALG_BYTES / (ms / 1e3) / 1e9, 1)
+    for mse in (False, True):  # the sequential error-term order, per-tensor scale
+        c = fos.Config(mse=mse, err_f16=True, seq_order=True)
+        ms = _graph_ms(rot(lambda i: fos.quantize(xs[i], c, amax=am[i], codes=codes,
+                                                  scales=scales)), R8, stream)
+        sweep[("mse" if mse else "mae") + "_f16_448_tensor_seq"] = round(
+            ALG_BYTES / (ms / 1e3) / 1e9, 1)
     res["encode_sweep_GB/s"] = sweep
     # a1+a8 with the row amax fused?  (row amax is a separate pass; both timed)
     ms = _graph_ms(rot(lambda i: fos.quantize(xs[i], fos.Config(row_scaled=True),
@@ -466,10 +472,22 @@ def _rows(fos, xs, stream, peak):
     ws_ = workloads.qdq_weights(8, 2048, 7168, seed=0, device=dev)
     wam = [fos.amax(t) for t in ws_]
     wout = [torch.empty_like(t) for t in ws_]
-    for mode in ("std", "mse_f16", "mae_f16"):
-        c = fos.Config(four_over_six=(mode != "std"), mse=(mode != "mae_f16"), err_f16=True)
+    for mode in ("std", "mse_f16", "mae_f16", "mse_f16_seq", "mae_f16_seq"):
+        c = fos.Config(four_over_six=(mode != "std"), mse=not mode.startswith("mae"),
+                       err_f16=True, seq_order=mode.endswith("_seq"))
         ms = _graph_ms(lambda: fos.qdq(ws_, c, amaxes=wam, outs=wout), 2, stream)
         rec("qdq_list_8x2048x7168_bf16_" + mode, sum(t.numel() for t in ws_) * 4, ms)
+    del ws_, wout
+    # the Megatron page's own benchmark shape: eight 4096x6144 bf16 weights,
+    # fused QDQ with the caller's amax and the sequential (TE) term order
+    ws_ = workloads.qdq_weights(8, 4096, 6144, seed=1, device=dev)
+    wam = [fos.amax(t) for t in ws_]
+    wout = [torch.empty_like(t) for t in ws_]
+    for mode in ("std", "mae_f16_seq", "mse_f16_seq"):
+        c = fos.Config(four_over_six=(mode != "std"), mse=not mode.startswith("mae"),
+                       err_f16=True, seq_order=mode.endswith("_seq"))
+        ms = _graph_ms(lambda: fos.qdq(ws_, c, amaxes=wam, outs=wout), 2, stream)
+        rec("qdq_list_8x4096x6144_bf16_" + mode, sum(t.numel() for t in ws_) * 4, ms)
     del ws_, wout
     # a11: dequantize back to bf16
     c = fos.Config()

@@ -69,14 +69,19 @@ def test_weight_16x16_full_size_sampled(dt):
 
 
 @pytest.mark.parametrize("dt", [torch.bfloat16, torch.float16])
-@pytest.mark.parametrize("mode", ["std", "mae_f16", "mse_f16", "mse"])
+@pytest.mark.parametrize("mode", ["std", "mae_f16", "mse_f16", "mse", "mae_f16_seq",
+                                  "mse_f16_seq"])
 def test_qdq_list_full_size_sampled(dt, mode):
     """Eight 2048x7168 weights, N(0, 0.02) with 0.1 % x30 outliers, with the
-    caller's FP32 per-tensor amax, fused QDQ of the whole list in one call."""
+    caller's FP32 per-tensor amax, fused QDQ of the whole list in one call
+    (the *_seq modes sum error terms in element order)."""
     four = mode != "std"
-    gcfg = fos.Config(four_over_six=four, mse=(mode != "mae_f16"), err_f16=mode.endswith("f16"))
-    ocfg = oracle.Config(four_over_six=four, mse=(mode != "mae_f16"),
-                         err_f16=mode.endswith("f16"), amax_is_input=True)
+    mse = not mode.startswith("mae")
+    f16 = "f16" in mode
+    seq = mode.endswith("_seq")
+    gcfg = fos.Config(four_over_six=four, mse=mse, err_f16=f16, seq_order=seq)
+    ocfg = oracle.Config(four_over_six=four, mse=mse, err_f16=f16, amax_is_input=True,
+                         seq_order=seq)
     ws = workloads.qdq_weights(8, 2048, 7168, seed=0, dtype=dt, device=DEV)
     host = [t.cpu().float().numpy() for t in ws]
     am = [oracle.amax_tensor(h) for h in host]
