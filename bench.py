@@ -477,6 +477,19 @@ def _rows(fos, xs, stream, peak):
                        err_f16=True, seq_order=mode.endswith("_seq"))
         ms = _graph_ms(lambda: fos.qdq(ws_, c, amaxes=wam, outs=wout), 2, stream)
         rec("qdq_list_8x2048x7168_bf16_" + mode, sum(t.numel() for t in ws_) * 4, ms)
+    # the same list with the per-tensor amax computed: separate amax passes
+    # then the QDQ launch, against one fused persistent launch (the bytes
+    # counted are the QDQ's, 4 per element, as above: strict)
+    c = fos.Config(err_f16=True, seq_order=True)
+    wsp = fos.qdq_fused_workspace(len(ws_), dev)
+    ms = _graph_ms(lambda: fos.qdq(ws_, c, amaxes=wam, outs=wout, amax_given=False), 2, stream)
+    rec("qdq_list_8x2048x7168_bf16_mse_f16_seq_amax_separate", sum(t.numel() for t in ws_) * 4,
+        ms)
+    ms = _graph_ms(lambda: fos.qdq_fused(ws_, c, amaxes=wam, outs=wout, workspace=wsp), 2,
+                   stream)
+    rec("qdq_list_8x2048x7168_bf16_mse_f16_seq_amax_fused", sum(t.numel() for t in ws_) * 4, ms)
+    if fos.workspace_error(wsp) != 0:
+        raise RuntimeError("fused QDQ: a wait between warps ran out")
     del ws_, wout
     # the Megatron page's own benchmark shape: eight 4096x6144 bf16 weights,
     # fused QDQ with the caller's amax and the sequential (TE) term order

@@ -187,6 +187,42 @@ FOS_API fos_status fos_qdq(int n, const void* const* x, void* const* out, const 
                    const fos_config* cfg, fos_stream_t stream);
 
 /*
+ * fos_qdq_fused -- fos_qdq with the per-tensor amax computed, in ONE
+ * persistent launch (the only other work on the stream is a clear of the
+ * workspace): the launch runs the amax pass of tensor 0, then
+ * quantize-dequantizes tensor i while it computes the amax of tensor i+1
+ * (the survey's "fused multi-tensor amax + QDQ in one persistent launch";
+ * the Megatron PR computes each weight's amax with a separate PyTorch
+ * reduction first).  Knobs, layouts and results are those of fos_qdq with
+ * cfg->amax_is_input = 0, which this call requires; amax[i] receives tensor
+ * i's amax.  n <= FOS_QDQ_MAX_LIST.
+ *   workspace: the warps of the launch wait for one another (a tensor's QDQ
+ *   starts once its amax is complete) and keep their counters here: device
+ *   memory owned by the caller, on the tensors' device, 256-byte aligned, at
+ *   least fos_qdq_fused_workspace_bytes(n) bytes.  The call clears it on
+ *   `stream` before the launch; calls that may run at the same time need
+ *   different workspaces.
+ * The launch is cooperative (all of its CTAs resident at once); it returns
+ * FOS_ERR_CUDA if the device cannot place them.  Every wait is bounded: one
+ * that does not complete within about a second ends the launch with the
+ * outputs incomplete and a nonzero code in the workspace, which
+ * fos_workspace_error reads.
+ */
+FOS_API size_t fos_qdq_fused_workspace_bytes(int n);
+FOS_API fos_status fos_qdq_fused(int n, const void* const* x, void* const* out,
+                                 const int64_t* rows, const int64_t* cols, float* const* amax,
+                                 fos_dtype dt, const fos_config* cfg, void* workspace,
+                                 size_t workspace_bytes, fos_stream_t stream);
+
+/*
+ * fos_workspace_error -- waits for `stream` to finish, then stores in *code
+ * the error word of a workspace used by fos_qdq_fused: 0 when no wait ran
+ * out, 1 when one did.  The one call of this library that synchronises the
+ * host (a diagnostic).
+ */
+FOS_API fos_status fos_workspace_error(const void* workspace, fos_stream_t stream, int* code);
+
+/*
  * fos_quantize_grouped -- one call over a packed MoE token tensor (grouped
  * PR, third commit: "each token group's amax expands to a per-row vector so
  * the whole packed tensor quantizes in one call, bitwise identical to

@@ -85,8 +85,12 @@ def lib():
         L.fos_qdq.argtypes = [I, P, P, P, P, P, I, CFG, P]
         L.fos_quantize_grouped.argtypes = [P, I, I64, I64, P, I, CFG, P, P, P, P]
         L.fos_diag_convert.argtypes = [I, P, P, I64, P]
+        L.fos_qdq_fused_workspace_bytes.argtypes = [I]
+        L.fos_qdq_fused_workspace_bytes.restype = ctypes.c_size_t
+        L.fos_qdq_fused.argtypes = [I, P, P, P, P, P, I, CFG, P, ctypes.c_size_t, P]
+        L.fos_workspace_error.argtypes = [P, P, ctypes.POINTER(I)]
         for n in ("fos_amax", "fos_quantize", "fos_quantize_list", "fos_quantize_overlap",
-                  "fos_dequantize", "fos_qdq",
+                  "fos_dequantize", "fos_qdq", "fos_qdq_fused", "fos_workspace_error",
                   "fos_quantize_grouped", "fos_diag_convert"):
             getattr(L, n).restype = ctypes.c_int
         L.fos_status_string.argtypes = [I]
@@ -247,6 +251,50 @@ def qdq(xs, cfg=Config(), amaxes=None, outs=None, amax_given=None):
     _check(lib().fos_qdq(n, xp, op, rows, cols, ap, _DT[dt], ctypes.byref(cc), _stream(xs[0])),
            "fos_qdq")
     return outs
+
+
+def qdq_fused_workspace(n, device):
+    """A workspace for fos_qdq_fused over n tensors (caller-side allocation)."""
+    nb = lib().fos_qdq_fused_workspace_bytes(int(n))
+    return torch.empty(max(nb, 256), dtype=torch.uint8, device=device)
+
+
+def qdq_fused(xs, cfg=Config(), amaxes=None, outs=None, workspace=None):
+    """fos_qdq_fused: amax of every tensor and the fused quantize-dequantize
+    of the list in one persistent launch.  amaxes (outputs) and outs are
+    allocated when None; workspace too (see qdq_fused_workspace).  Returns
+    (outs, amaxes)."""
+    n = len(xs)
+    if n == 0:
+        return [], []
+    for x in xs:
+        _cuda(x, "x")
+    dev = xs[0].device
+    if amaxes is None:
+        amaxes = [torch.empty(1, dtype=torch.float32, device=dev) for _ in xs]
+    if outs is None:
+        outs = [torch.empty_like(x) for x in xs]
+    if workspace is None:
+        workspace = qdq_fused_workspace(n, dev)
+    P = ctypes.c_void_p * n
+    xp = P(*[x.data_ptr() for x in xs])
+    op = P(*[o.data_ptr() for o in outs])
+    ap = P(*[a.data_ptr() for a in amaxes])
+    rows = (ctypes.c_int64 * n)(*[x.shape[0] for x in xs])
+    cols = (ctypes.c_int64 * n)(*[x.shape[1] for x in xs])
+    cc = cfg.c(False)
+    _check(lib().fos_qdq_fused(n, xp, op, rows, cols, ap, _DT[xs[0].dtype], ctypes.byref(cc),
+                               _p(workspace), workspace.numel(), _stream(xs[0])),
+           "fos_qdq_fused")
+    return outs, amaxes
+
+
+def workspace_error(workspace):
+    """The error word of a fused-launch workspace (waits for the stream)."""
+    code = ctypes.c_int(0)
+    _check(lib().fos_workspace_error(_p(workspace), _stream(workspace), ctypes.byref(code)),
+           "fos_workspace_error")
+    return code.value
 
 
 def quantize_grouped(x, offs, cfg=Config(), group_amax=None, codes=None, scales=None,

@@ -610,3 +610,91 @@ fos_status fos_diag_convert(int op, const void* in, void* out, int64_t n, fos_st
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------ fused amax + QDQ
+extern "C" {
+
+size_t fos_qdq_fused_workspace_bytes(int n) {
+    if (n <= 0) return 0;
+    const size_t words = 1 + 2 * (size_t)n;  // error word, n counters, n running amaxes
+    return (words * sizeof(uint32_t) + 255) / 256 * 256;
+}
+
+fos_status fos_qdq_fused(int n, const void* const* x, void* const* out, const int64_t* rows,
+                         const int64_t* cols, float* const* amax, fos_dtype dt,
+                         const fos_config* cfg, void* workspace, size_t workspace_bytes,
+                         fos_stream_t stream) {
+    if (n < 0) return FOS_ERR_INVALID_ARG;
+    if (dt != FOS_BF16 && dt != FOS_FP16) return valid_dtype(dt) ? FOS_ERR_UNSUPPORTED
+                                                                  : FOS_ERR_INVALID_ARG;
+    fos_status st = check_config(cfg);
+    if (st) return st;
+    if (cfg->block != FOS_BLOCK_1X16 || cfg->granularity != FOS_SCALE_TENSOR ||
+        cfg->amax_is_input)
+        return FOS_ERR_UNSUPPORTED;
+    if (n > kQdqMaxList) return FOS_ERR_UNSUPPORTED;
+    if (n == 0) return FOS_OK;
+    if (!x || !out || !rows || !cols || !amax || !workspace) return FOS_ERR_INVALID_ARG;
+    const size_t need = fos_qdq_fused_workspace_bytes(n);
+    if (workspace_bytes < need) return FOS_ERR_INVALID_ARG;
+    if (!aligned(workspace, 256)) return FOS_ERR_MISALIGNED;
+    for (int i = 0; i < n; ++i) {
+        st = check_shape(rows[i], cols[i], false);
+        if (st) return st;
+        const bool empty = rows[i] == 0 || cols[i] == 0;
+        if (!amax[i] || (!empty && (!x[i] || !out[i]))) return FOS_ERR_INVALID_ARG;
+        if (!empty && (!aligned(x[i], 32) || !aligned(out[i], 32))) return FOS_ERR_MISALIGNED;
+    }
+    int dev = device_of(workspace);
+    if (dev < 0) return FOS_ERR_INVALID_ARG;
+    for (int i = 0; i < n; ++i) {
+        const bool empty = rows[i] == 0 || cols[i] == 0;
+        const int d = empty ? common_device({amax[i]}) : common_device({x[i], out[i], amax[i]});
+        if (d != dev) return FOS_ERR_INVALID_ARG;
+    }
+    DeviceScope scope(dev);
+    if (scope.st) return scope.st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    QdqFusedArgs a;
+    std::memset(&a, 0, sizeof(a));
+    a.q.n = n;
+    a.q.six_bound = 6.0f * (float)cfg->e4m3_bound;
+    a.q.neg_zero = -0.0f;
+    int64_t u = 0;
+    for (int i = 0; i < n; ++i) {
+        QdqTensor& t = a.q.t[i];
+        t.x = x[i];
+        t.out = out[i];
+        t.nblk = rows[i] * (cols[i] / 16);
+        t.unit_begin = u;
+        u += (t.nblk + 31) / 32;
+        a.amax_out[i] = amax[i];
+    }
+    a.q.t[n].unit_begin = u;
+    a.q.units = u;
+    uint32_t* w = static_cast<uint32_t*>(workspace);
+    a.ws.err = w;
+    a.ws.cnt = w + 1;
+    a.ws.acc = w + 1 + n;
+    st = cuda_status(cudaMemsetAsync(workspace, 0, need, s));
+    if (st) return st;
+    return cuda_status(launch_qdq_fused(in_of(dt), err_of(cfg), a, s));
+}
+
+fos_status fos_workspace_error(const void* workspace, fos_stream_t stream, int* code) {
+    if (!workspace || !code) return FOS_ERR_INVALID_ARG;
+    const int dev = device_of(workspace);
+    if (dev < 0) return FOS_ERR_INVALID_ARG;
+    DeviceScope scope(dev);
+    if (scope.st) return scope.st;
+    fos_status st = cuda_status(cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)));
+    if (st) return st;
+    uint32_t v = 0;
+    st = cuda_status(cudaMemcpy(&v, workspace, sizeof(v), cudaMemcpyDeviceToHost));
+    if (st) return st;
+    *code = (int)v;
+    return FOS_OK;
+}
+
+}  // extern "C"
+

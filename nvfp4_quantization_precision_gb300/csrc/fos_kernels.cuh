@@ -370,6 +370,162 @@ __global__ void __launch_bounds__(kThreads, min_ctas<EM>()) k_qdq1x16(const __gr
 }
 
 // ------------------------------------------------------------------------
+// Fused multi-tensor amax + QDQ in one persistent launch.  The launch first
+// runs the amax pass of tensor 0 with every warp; then, for each tensor i,
+// it quantize-dequantizes tensor i while every warp folds one segment of
+// tensor i+1 into its running max per step (as the list pipeline does).  A
+// CTA starts the QDQ of tensor i once every CTA of the grid has finished its
+// share of tensor i's amax: a CTA max-reduces its warps' maxima, atomicMax-es
+// the result into the workspace and then adds 1 to the tensor's counter with
+// release semantics; one thread per CTA polls the counter with acquire loads
+// (backing off with nanosleep) until it holds the number of CTAs and hands
+// the amax to the other threads through shared memory.  The launch is
+// cooperative (all CTAs resident at once) and no CTA leaves early, so every
+// counter fills; a wait still gives up after kWaitSpins polls (about a
+// second), records kWsTimeout in the workspace and ends its CTA, and a CTA
+// that sees a recorded failure stops waiting too.
+// ------------------------------------------------------------------------
+constexpr uint32_t kWaitSpins = 1u << 20;  // polls of up to about 1 us each
+constexpr uint32_t kWsTimeout = 1u;        // workspace error code: a wait ran out
+
+// Workspace of the fused launch (device memory, cleared before the launch):
+// word 0 the error code, then n counters, then n running amaxes (float bits).
+struct FusedWs {
+    uint32_t* err;
+    uint32_t* cnt;
+    uint32_t* acc;
+};
+
+struct QdqFusedArgs {
+    QdqArgs q;                       // t[i].amax unused; amax_out receives the amaxes
+    float* amax_out[kQdqMaxList];
+    FusedWs ws;
+};
+
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void red_release_add_gpu(uint32_t* p, uint32_t v) {
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// The CTA's share of one tensor's amax is done: max into the running amax,
+// then count the CTA in (release orders the max before the count).  Every
+// thread of the CTA calls it.
+__device__ __forceinline__ void fused_arrive(float m, uint32_t* acc, uint32_t* cnt, float* s_red,
+                                             int warp, int lane) {
+    m = warp_max_dev(m);
+    if (lane == 0) s_red[warp] = m;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float c = 0.0f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) c = fmaxf(c, s_red[w]);
+        if (c > 0.0f) atomicMax(acc, __float_as_uint(c));
+        red_release_add_gpu(cnt, 1u);
+    }
+}
+
+// Wait until *cnt reaches target (every thread of the CTA calls it); returns
+// the tensor's amax, or a negative value when the wait gave up (the error is
+// then recorded).
+__device__ __forceinline__ float fused_wait(const uint32_t* cnt, const uint32_t* acc,
+                                            uint32_t target, uint32_t* err, float* s_amax) {
+    if (threadIdx.x == 0) {
+        float A = -1.0f;
+        uint32_t spins = 0, sleep = 32;
+        for (;;) {
+            if (ld_acquire_gpu(cnt) >= target) {
+                A = __uint_as_float(ld_acquire_gpu(acc));
+                break;
+            }
+            if (ld_acquire_gpu(err) != 0u || ++spins > kWaitSpins) {
+                atomicCAS(err, 0u, kWsTimeout);
+                break;
+            }
+            __nanosleep(sleep);
+            if (sleep < 1024) sleep *= 2;
+        }
+        *s_amax = A;
+    }
+    __syncthreads();
+    return *s_amax;
+}
+
+template <In IT, Err EM>
+__global__ void __launch_bounds__(kThreads, min_ctas<EM>())
+    k_qdq_fused(const __grid_constant__ QdqFusedArgs a) {
+    static_assert(IT != In::F32, "fused QDQ is bf16 / fp16 only");
+    constexpr Out OT = (IT == In::BF16) ? Out::BF16 : Out::F16;
+    constexpr int64_t kBytes = 32;
+    __shared__ float2 s_tbl[kWarps][128];
+    __shared__ float s_red[kWarps];
+    __shared__ float s_amax;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    float2* tbl = s_tbl[warp];
+    const uint64_t nz = pk(a.q.neg_zero, a.q.neg_zero);
+    const int64_t nw = (int64_t)gridDim.x * kWarps;
+    const int64_t step = nw * 32;
+    const int64_t b0 = ((int64_t)blockIdx.x * kWarps + warp) * 32 + lane;
+    {  // amax pass of tensor 0
+        const char* ab = static_cast<const char*>(a.q.t[0].x);
+        const int64_t aseg = a.q.t[0].nblk;
+        float m = 0.0f;
+        for (int64_t b = b0; b < aseg + lane; b += step) {  // b - lane: first segment of unit
+            Raw<IT> r;
+            zero_seg<IT>(r);
+            if (b < aseg) load_seg<IT, kAmaxHint>(r, ab + b * kBytes);
+            uint64_t xq[8];
+            widen<IT>(r, xq);
+            m = fmaxf(m, seg_amax(xq));
+        }
+        fused_arrive(m, &a.ws.acc[0], &a.ws.cnt[0], s_red, warp, lane);
+    }
+    for (int s = 0; s < a.q.n; ++s) {
+        const float A = fused_wait(&a.ws.cnt[s], &a.ws.acc[s], gridDim.x, a.ws.err, &s_amax);
+        if (A < 0.0f) return;  // the wait gave up (the whole CTA leaves); failure recorded
+        if (blockIdx.x == 0 && threadIdx.x == 0) *a.amax_out[s] = A;
+        const float S = global_scale(A, a.q.six_bound);
+        build_table(tbl, S, lane);
+        const QdqTensor& T = a.q.t[s];
+        const char* xb = static_cast<const char*>(T.x);
+        char* ob = static_cast<char*>(T.out);
+        const bool next = s + 1 < a.q.n;
+        const char* ab = next ? static_cast<const char*>(a.q.t[s + 1].x) : nullptr;
+        const int64_t aseg = next ? a.q.t[s + 1].nblk : 0;
+        const int64_t nmax = T.nblk > aseg ? T.nblk : aseg;
+        Raw<IT> buf[2];
+        load_if<IT, kQdqHint>(buf[0], xb + b0 * kBytes, b0 < T.nblk);
+        float m = 0.0f;
+        for (int64_t b = b0; b < nmax + lane; b += 2 * step) {
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                const int64_t bl = b + (k + 1) * step;
+                load_if<IT, kQdqHint>(buf[(k + 1) % 2], xb + bl * kBytes, bl < T.nblk);
+                const int64_t bc = b + k * step;
+                Raw<IT> ra;
+                zero_seg<IT>(ra);
+                if (bc < aseg) load_seg<IT, kAmaxHint>(ra, ab + bc * kBytes);
+                if (bc < T.nblk) {
+                    uint64_t xp[8];
+                    widen<IT>(buf[k], xp);
+                    uint32_t code[2], scale, out[8];
+                    encode_block<EM, OT>(xp, S, tbl, nz, code, scale, out);
+                    st256(ob + bc * kBytes, out);
+                }
+                uint64_t xq[8];
+                widen<IT>(ra, xq);
+                m = fmaxf(m, seg_amax(xq));
+            }
+        }
+        if (next) fused_arrive(m, &a.ws.acc[s + 1], &a.ws.cnt[s + 1], s_red, warp, lane);
+    }
+}
+
+
+// ------------------------------------------------------------------------
 // 16x16 quantize.  Unit = (band of 16 rows, quad of four 16x16 tiles); lane l
 // holds rows (l >> 2) and (l >> 2) + 8 of tile 4 * quad + (l & 3), so each
 // warp load reads eight whole 4-tile row spans.  Each CTA takes a contiguous

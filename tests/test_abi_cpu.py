@@ -176,3 +176,35 @@ def test_quantize_overlap_requires_given_per_tensor_1x16(L):
         fos.FOS_ERR_MISALIGNED
     assert L.fos_quantize_overlap(FAKE, 0, 16, 16, ctypes.byref(c), FAKE, FAKE, FAKE, FAKE,
                                   16, 20, FAKE, None) == fos.FOS_ERR_UNSUPPORTED
+
+
+def test_qdq_fused_workspace_size(L):
+    assert L.fos_qdq_fused_workspace_bytes(0) == 0
+    assert L.fos_qdq_fused_workspace_bytes(1) == 256
+    assert L.fos_qdq_fused_workspace_bytes(64) == 768  # (1 + 2 * 64) words, rounded to 256 B
+
+
+def test_qdq_fused_rejects_before_any_cuda_call(L):
+    P1 = ctypes.c_void_p * 1
+    x, o, a = P1(FAKE), P1(FAKE), P1(FAKE)
+    rows, cols = (ctypes.c_int64 * 1)(16), (ctypes.c_int64 * 1)(16)
+    ws = ctypes.c_void_p(0x100000)
+
+    def call(n=1, cfg=None, w=ws, nbytes=256, dt=0):
+        c = cfg or _cfg(amax_is_input=0)
+        return L.fos_qdq_fused(n, x, o, rows, cols, a, dt, ctypes.byref(c), w, nbytes, None)
+    assert call(cfg=_cfg(amax_is_input=1)) == fos.FOS_ERR_UNSUPPORTED  # the amax is computed
+    assert call(cfg=_cfg(amax_is_input=0, block=1)) == fos.FOS_ERR_UNSUPPORTED
+    assert call(cfg=_cfg(amax_is_input=0, granularity=1)) == fos.FOS_ERR_UNSUPPORTED
+    assert call(dt=2) == fos.FOS_ERR_UNSUPPORTED                      # fp32
+    assert call(n=65) == fos.FOS_ERR_UNSUPPORTED                       # above FOS_QDQ_MAX_LIST
+    assert call(n=-1) == fos.FOS_ERR_INVALID_ARG
+    assert call(w=None) == fos.FOS_ERR_INVALID_ARG
+    assert call(nbytes=255) == fos.FOS_ERR_INVALID_ARG                 # workspace too small
+    assert call(w=ctypes.c_void_p(0x100080)) == fos.FOS_ERR_MISALIGNED
+    assert call(n=0) == fos.FOS_OK
+
+
+def test_workspace_error_rejects_null(L):
+    code = ctypes.c_int(7)
+    assert L.fos_workspace_error(None, None, ctypes.byref(code)) == fos.FOS_ERR_INVALID_ARG

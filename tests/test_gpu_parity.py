@@ -584,3 +584,42 @@ def test_seq_order_with_16x16_is_unsupported():
         fos.quantize(x, fos.Config(block16x16=True, seq_order=True))
     # standard mode has no candidate errors, so the order is moot and accepted
     fos.quantize(x, fos.Config(block16x16=True, four_over_six=False, seq_order=True))
+
+
+# ------------------------------------------------------------------ fused amax + QDQ
+@pytest.mark.parametrize("dt", ["bf16", "f16"])
+@pytest.mark.parametrize("mode,seq", [("std", False), ("mse", False), ("mae_f16", False),
+                                      ("mse_f16", False), ("mae_f16", True), ("mse", True)])
+def test_qdq_fused(dt, mode, seq):
+    """One persistent launch computes every amax and the QDQ of the list
+    (empty and ragged entries included); two calls in a row on the same
+    workspace give the oracle's bytes both times."""
+    gcfg, ocfg = _cfgs(mode, 448, seq=seq)
+    shapes = [(64, 1024), (0, 64), (7, 1040), (300, 2064), (48, 272), (1, 16)]
+    xs = [workloads.qdq_weights(1, r, c, seed=90 + i, dtype=DTYPES[dt])[0] if r else
+          torch.zeros(0, c, dtype=DTYPES[dt]) for i, (r, c) in enumerate(shapes)]
+    xd = [x.to(DEV) for x in xs]
+    ws = fos.qdq_fused_workspace(len(xd), DEV)
+    for _ in range(2):
+        outs, amaxes = fos.qdq_fused(xd, gcfg, workspace=ws)
+        assert fos.workspace_error(ws) == 0
+        for x, o, a in zip(xs, outs, amaxes):
+            ref, oa = oracle.qdq(x.float().numpy(), ocfg, dt)
+            assert np.array_equal(_u32(a), oa.view(np.uint32))
+            if x.numel():
+                assert np.array_equal(_u16(o), ref)
+
+
+def test_qdq_fused_equals_separate_amax_passes_full_size():
+    """8 x 2048x7168 bf16 (the fake-QAT weight list): the fused launch gives
+    the bytes of fos_qdq with the amax computed by separate passes."""
+    xs = workloads.qdq_weights(8, 2048, 7168, seed=3, device=DEV)
+    for mode in ("mse_f16", "std"):
+        gcfg, _ = _cfgs(mode, 448, seq=(mode != "std"))
+        outs, amaxes = fos.qdq_fused(xs, gcfg)
+        ref = fos.qdq(xs, gcfg, amax_given=False)
+        a2 = [fos.amax(x) for x in xs]
+        torch.cuda.synchronize()
+        for o, r, a, b in zip(outs, ref, amaxes, a2):
+            assert torch.equal(o.view(torch.int16), r.view(torch.int16))
+            assert torch.equal(a, b)
