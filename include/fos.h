@@ -215,6 +215,31 @@ FOS_API fos_status fos_qdq_fused(int n, const void* const* x, void* const* out,
                                  size_t workspace_bytes, fos_stream_t stream);
 
 /*
+ * fos_qdq_fused_static -- fos_qdq_fused without a workspace argument, for
+ * callers that have no way to obtain device memory at the point of the call:
+ * code that runs inside another framework's allocator and may not go around
+ * it, or a runtime that forbids allocations after its start-up.  The pages
+ * have no counterpart; this is a convenience of this library.
+ * The counters live in one fixed array of the library (768 bytes on every
+ * GPU that loads it, kept until the process exits), so lists are limited to
+ * n <= FOS_QDQ_MAX_LIST (64); longer lists return FOS_ERR_UNSUPPORTED.
+ * Nothing is allocated: no cudaMalloc, no cudaFree, no allocating library
+ * call.  The first call on a device looks up the array's device address
+ * (with that device current) and caches it; make that first call before any
+ * stream capture.  Each call clears the array on `stream` before its launch.
+ * Every call on a device shares the one array: calls whose work may overlap
+ * on the GPU (other streams, other threads) race and give wrong results;
+ * order them on one stream.  A wait that runs out is recorded in the array
+ * (not readable through this call); use fos_qdq_fused with a workspace of
+ * your own when that must be checked.  Arguments, results and errors are
+ * otherwise those of fos_qdq_fused.
+ */
+FOS_API fos_status fos_qdq_fused_static(int n, const void* const* x, void* const* out,
+                                        const int64_t* rows, const int64_t* cols,
+                                        float* const* amax, fos_dtype dt,
+                                        const fos_config* cfg, fos_stream_t stream);
+
+/*
  * fos_workspace_error -- waits for `stream` to finish, then stores in *code
  * the error word of a workspace used by fos_qdq_fused: 0 when no wait ran
  * out, 1 when one did.  The one call of this library that synchronises the
