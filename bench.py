@@ -461,6 +461,19 @@ def _rows(fos, xs, stream, peak):
     ms = _graph_ms(rot(lambda i: fos.quantize(xs[i], fos.Config(row_scaled=True),
                                               codes=codes, scales=scales)), R8, stream)
     rec("encode_row_scaled_with_amax_pass", ALG_BYTES, ms)
+    # the column-wise operand (x^T) alone and with the row-wise result of
+    # the same read, 4/6 MSE, amax given
+    ct = torch.empty(COLS, ROWS // 2, dtype=torch.uint8, device=dev)
+    st_ = torch.empty(COLS, ROWS // 16, dtype=torch.uint8, device=dev)
+    c = fos.Config()
+    ms = _graph_ms(rot(lambda i: fos.quantize_colwise(xs[i], c, amax=am[i], codes_t=ct,
+                                                      scales_t=st_)), R8, stream)
+    rec("colwise_8192x4096_bf16_mse", ALG_BYTES, ms)
+    ms = _graph_ms(rot(lambda i: fos.quantize_colwise(xs[i], c, amax=am[i], codes_t=ct,
+                                                      scales_t=st_, codes=codes, scales=scales)),
+                   R8, stream)
+    rec("colwise_and_rowwise_8192x4096_bf16_mse", ELEMS * (2 + 2 * (0.5 + 1 / 16)), ms)
+    del ct, st_
     # a9: fused QDQ at the metric shape and on the 8 x 2048x7168 weight list
     outs4 = [torch.empty_like(x) for x in xs]
     for mode in ("std", "mse_f16", "mse_exact"):

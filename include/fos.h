@@ -155,6 +155,26 @@ FOS_API fos_status fos_quantize_overlap(const void* x, fos_dtype dt, int64_t row
                                         float* amax_next, fos_stream_t stream);
 
 /*
+ * fos_quantize_colwise -- the column-wise operand: fos_quantize applied to
+ * x^T ([cols, rows]), computed from the row-major x [rows, cols] without
+ * forming x^T.  Blocks are 16 consecutive rows of one column of x:
+ *   codes_t [cols, rows/2], scales_t [cols, rows/16] (row c of x^T = column
+ *   c of x, low nibble = the upper of two rows).
+ * With codes and scales both non-NULL the row-wise result of x ([rows,
+ * cols/2], [rows, cols/16], exactly fos_quantize's) is written by the same
+ * launch from the same read of x; both NULL skips it.  1x16 blocks and a
+ * per-tensor scale only (the amax of x and of x^T are the same value);
+ * rows % 16 == 0 and cols % 16 == 0.  amax as in fos_quantize.  The pages
+ * list transpose / column-wise output as a non-goal of their QDQ path (the
+ * Megatron PR's deliberate non-goals); this is the layout a weight-gradient
+ * GEMM reads, built with the same arithmetic.
+ */
+FOS_API fos_status fos_quantize_colwise(const void* x, fos_dtype dt, int64_t rows, int64_t cols,
+                                        const fos_config* cfg, float* amax, uint8_t* codes_t,
+                                        uint8_t* scales_t, uint8_t* codes, uint8_t* scales,
+                                        fos_stream_t stream);
+
+/*
  * fos_dequantize -- standard NVFP4 decode (grouped PR, first commit:
  * "nvfp4_dequantize: the standard NVFP4 decode (recipe-agnostic)"):
  *   out = round_to(out_dt, e2m1(code) * (e4m3(scale) / S)),

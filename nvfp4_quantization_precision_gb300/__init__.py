@@ -253,6 +253,43 @@ def qdq(xs, cfg=Config(), amaxes=None, outs=None, amax_given=None):
     return outs
 
 
+def quantize_colwise(x, cfg=Config(), amax=None, codes_t=None, scales_t=None, rowwise=False,
+                     codes=None, scales=None, amax_given=None):
+    """fos_quantize_colwise: the quantization of x.T from x (1x16, per-tensor
+    scale).  With rowwise=True (or codes/scales passed) the row-wise result
+    of x comes from the same read.  Returns (codes_t, scales_t, amax) or
+    (codes_t, scales_t, amax, codes, scales)."""
+    _cuda(x, "x")
+    R, C = x.shape
+    dev = x.device
+    given = (amax is not None) if amax_given is None else bool(amax_given)
+    if amax is None:
+        amax = torch.empty(1, dtype=torch.float32, device=dev)
+    if codes_t is None:
+        codes_t = torch.empty((C, R // 2), dtype=torch.uint8, device=dev)
+    if scales_t is None:
+        scales_t = torch.empty((C, R // 16), dtype=torch.uint8, device=dev)
+    dual = rowwise or codes is not None or scales is not None
+    if dual and codes is None:
+        codes = torch.empty((R, C // 2), dtype=torch.uint8, device=dev)
+    if dual and scales is None:
+        scales = torch.empty((R, C // 16), dtype=torch.uint8, device=dev)
+    L = lib()
+    if not getattr(L, "_colwise_declared", False):
+        P, I64, I = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+        L.fos_quantize_colwise.argtypes = [P, I, I64, I64, ctypes.POINTER(FosConfig), P, P, P, P,
+                                           P, P]
+        L.fos_quantize_colwise.restype = I
+        L._colwise_declared = True
+    cc = cfg.c(given)
+    _check(L.fos_quantize_colwise(_p(x), _DT[x.dtype], R, C, ctypes.byref(cc), _p(amax),
+                                  _p(codes_t), _p(scales_t), _p(codes), _p(scales), _stream(x)),
+           "fos_quantize_colwise")
+    if dual:
+        return codes_t, scales_t, amax, codes, scales
+    return codes_t, scales_t, amax
+
+
 def qdq_fused_workspace(n, device):
     """A workspace for fos_qdq_fused over n tensors (caller-side allocation)."""
     nb = lib().fos_qdq_fused_workspace_bytes(int(n))

@@ -698,3 +698,62 @@ fos_status fos_workspace_error(const void* workspace, fos_stream_t stream, int* 
 
 }  // extern "C"
 
+// ------------------------------------------------------------ column-wise quantize
+extern "C" {
+
+fos_status fos_quantize_colwise(const void* x, fos_dtype dt, int64_t rows, int64_t cols,
+                                const fos_config* cfg, float* amax, uint8_t* codes_t,
+                                uint8_t* scales_t, uint8_t* codes, uint8_t* scales,
+                                fos_stream_t stream) {
+    if (!valid_dtype(dt)) return FOS_ERR_INVALID_ARG;
+    fos_status st = check_config(cfg);
+    if (st) return st;
+    if (cfg->block != FOS_BLOCK_1X16 || cfg->granularity != FOS_SCALE_TENSOR)
+        return FOS_ERR_UNSUPPORTED;
+    st = check_shape(rows, cols, false);
+    if (st) return st;
+    st = check_shape(cols, rows, false);  // x^T: blocks run down the rows
+    if (st) return st;
+    if ((codes == nullptr) != (scales == nullptr)) return FOS_ERR_INVALID_ARG;
+    const bool dual = codes != nullptr;
+    if (!amax) return FOS_ERR_INVALID_ARG;
+    if (rows == 0 || cols == 0) {
+        if (cfg->amax_is_input) return FOS_OK;
+        const int d = device_of(amax);
+        if (d < 0) return FOS_ERR_INVALID_ARG;
+        DeviceScope scope(d);
+        if (scope.st) return scope.st;
+        return cuda_status(cudaMemsetAsync(amax, 0, sizeof(float),
+                                           reinterpret_cast<cudaStream_t>(stream)));
+    }
+    if (!x || !codes_t || !scales_t) return FOS_ERR_INVALID_ARG;
+    if (!aligned(x, 32) || !aligned(codes_t, 8) || (dual && !aligned(codes, 8)))
+        return FOS_ERR_MISALIGNED;
+    const int dev = dual ? common_device({x, amax, codes_t, scales_t, codes, scales})
+                         : common_device({x, amax, codes_t, scales_t});
+    if (dev < 0) return FOS_ERR_INVALID_ARG;
+    DeviceScope scope(dev);
+    if (scope.st) return scope.st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (!cfg->amax_is_input) {
+        st = cuda_status(run_amax(x, dt, rows, cols, Src::TENSOR, amax, nullptr, 0, s));
+        if (st) return st;
+    }
+    ColArgs a{};
+    a.x = x;
+    a.codes_t = codes_t;
+    a.scales_t = scales_t;
+    a.codes = codes;
+    a.scales = scales;
+    a.amax = amax;
+    a.rows = rows;
+    a.cols = cols;
+    a.tiles_c = (cols + kColTileC - 1) / kColTileC;
+    a.tiles = ((rows + kColTileR - 1) / kColTileR) * a.tiles_c;
+    a.six_bound = 6.0f * (float)cfg->e4m3_bound;
+    a.neg_zero = -0.0f;
+    return cuda_status(launch_colwise(in_of(dt), err_of(cfg), dual, a, s));
+}
+
+}  // extern "C"
+

@@ -370,6 +370,121 @@ __global__ void __launch_bounds__(kThreads, min_ctas<EM>()) k_qdq1x16(const __gr
 }
 
 // ------------------------------------------------------------------------
+// Column-wise quantize: the 1x16 quantization of x^T, computed from the
+// row-major x without forming x^T (the operand layout a weight-gradient
+// GEMM reads).  A CTA stages a tile of 64 rows x 256 columns in shared
+// memory: each thread loads four 16-element row segments (and, with DUAL,
+// encodes them row-wise straight from registers, so one read of x gives
+// both layouts).  Then thread c encodes the four 16-row blocks of tile
+// column c and writes 32 consecutive code bytes and 4 scale bytes of row c
+// of x^T.  Tiles are walked grid-stride; the scale is per tensor (x and x^T
+// have one amax).
+// ------------------------------------------------------------------------
+constexpr int kColTileR = 64, kColTileC = 256;
+
+struct ColArgs {
+    const void* x;
+    uint8_t* codes_t;   // [cols, rows / 2]
+    uint8_t* scales_t;  // [cols, rows / 16]
+    uint8_t* codes;     // DUAL: [rows, cols / 2]
+    uint8_t* scales;    // DUAL: [rows, cols / 16]
+    const float* amax;  // [1]
+    int64_t rows, cols;
+    int64_t tiles_c;    // tiles across the columns
+    int64_t tiles;
+    float six_bound;
+    float neg_zero;
+};
+
+template <In IT>
+__device__ __forceinline__ void store_seg_smem(unsigned char* p, const Raw<IT>& r) {
+    uint4* q = reinterpret_cast<uint4*>(p);
+#pragma unroll
+    for (int i = 0; i < InTraits<IT>::kWords / 4; ++i)
+        q[i] = make_uint4(r.w[4 * i], r.w[4 * i + 1], r.w[4 * i + 2], r.w[4 * i + 3]);
+}
+
+// Elements (rb*16 .. rb*16+15, column c) of the staged tile as one segment.
+template <In IT>
+__device__ __forceinline__ void gather_col(const unsigned char* tile, int rb, int c, Raw<IT>& r) {
+    if constexpr (IT == In::F32) {
+        const uint32_t* t = reinterpret_cast<const uint32_t*>(tile);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) r.w[i] = t[(rb * 16 + i) * kColTileC + c];
+    } else {
+        const uint16_t* t = reinterpret_cast<const uint16_t*>(tile);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const uint32_t lo = t[(rb * 16 + 2 * j) * kColTileC + c];
+            const uint32_t hi = t[(rb * 16 + 2 * j + 1) * kColTileC + c];
+            r.w[j] = lo | (hi << 16);
+        }
+    }
+}
+
+template <In IT, Err EM, bool DUAL>
+__global__ void __launch_bounds__(kThreads, min_ctas<EM>()) k_quant_colwise(const ColArgs a) {
+    chain_wait();
+    chain_release();
+    constexpr int64_t kElt = (IT == In::F32) ? 4 : 2;
+    extern __shared__ __align__(16) unsigned char s_tile[];  // kColTileR x kColTileC elements
+    __shared__ float2 s_tbl[kWarps][128];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    float2* tbl = s_tbl[warp];
+    const uint64_t nz = pk(a.neg_zero, a.neg_zero);
+    const float S = global_scale(a.amax[0], a.six_bound);
+    build_table(tbl, S, lane);
+    const char* xb = static_cast<const char*>(a.x);
+    const int64_t nb_t = a.rows / 16;  // blocks per row of x^T
+    uint32_t dummy[8];
+    for (int64_t tile = blockIdx.x; tile < a.tiles; tile += gridDim.x) {
+        const int64_t r0 = (tile / a.tiles_c) * kColTileR, c0 = (tile % a.tiles_c) * kColTileC;
+#pragma unroll
+        for (int k = 0; k < (kColTileR * kColTileC / 16) / kThreads; ++k) {
+            const int seg = tid + kThreads * k;
+            const int tr = seg >> 4, ts = seg & 15;  // tile row, 16-column segment
+            const int64_t row = r0 + tr, col = c0 + ts * 16;
+            const bool v = row < a.rows && col < a.cols;
+            Raw<IT> raw;
+            zero_seg<IT>(raw);
+            if (v) load_seg<IT, kEncHint>(raw, xb + (row * a.cols + col) * kElt);
+            store_seg_smem<IT>(s_tile + ((int64_t)tr * kColTileC + ts * 16) * kElt, raw);
+            if constexpr (DUAL) {
+                if (v) {
+                    uint64_t xp[8];
+                    widen<IT>(raw, xp);
+                    uint32_t code[2], scale;
+                    encode_block<EM, Out::NONE>(xp, S, tbl, nz, code, scale, dummy);
+                    const int64_t b = row * (a.cols / 16) + col / 16;
+                    st64(a.codes + b * 8, code[0], code[1]);
+                    st8(a.scales + b, scale);
+                }
+            }
+        }
+        __syncthreads();
+        const int64_t col = c0 + tid;  // one tile column per thread
+        if (col < a.cols) {
+#pragma unroll
+            for (int rb = 0; rb < kColTileR / 16; ++rb) {
+                const int64_t row = r0 + rb * 16;  // rows % 16 == 0: a block is whole or absent
+                if (row < a.rows) {
+                    Raw<IT> raw;
+                    gather_col<IT>(s_tile, rb, tid, raw);
+                    uint64_t xp[8];
+                    widen<IT>(raw, xp);
+                    uint32_t code[2], scale;
+                    encode_block<EM, Out::NONE>(xp, S, tbl, nz, code, scale, dummy);
+                    const int64_t b = col * nb_t + row / 16;
+                    st64(a.codes_t + b * 8, code[0], code[1]);
+                    st8(a.scales_t + b, scale);
+                }
+            }
+        }
+        __syncthreads();  // the tile buffer is refilled next
+    }
+}
+
+// ------------------------------------------------------------------------
 // Fused multi-tensor amax + QDQ in one persistent launch.  The launch first
 // runs the amax pass of tensor 0 with every warp; then, for each tensor i,
 // it quantize-dequantizes tensor i while every warp folds one segment of
@@ -528,7 +643,8 @@ __global__ void __launch_bounds__(kThreads, min_ctas<EM>())
 // ------------------------------------------------------------------------
 // 16x16 quantize.  Unit = (band of 16 rows, quad of four 16x16 tiles); lane l
 // holds rows (l >> 2) and (l >> 2) + 8 of tile 4 * quad + (l & 3), so each
-// warp load reads eight whole 4-tile row spans.  Each CTA takes a contiguous
+// warp load reads eight whole 4-tile row spans.  With a per-tensor scale the
+// warps walk the units grid-stride; otherwise each CTA takes a contiguous
 // range of units and its warps interleave inside it (neighbouring warps read
 // neighbouring spans; the band, and with it a per-row or per-group scale,
 // changes rarely for any one warp).  The next unit is loaded one step ahead.
@@ -543,9 +659,16 @@ __global__ void __launch_bounds__(kThreads, tile_min_ctas<IT>()) k_quant16x16(co
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     float2* tbl = s_tbl[warp];
     const uint64_t nz = pk(a.neg_zero, a.neg_zero);
-    const int64_t c1 = split_at(a.units, gridDim.x, blockIdx.x + 1);
-    const int64_t u0 = split_at(a.units, gridDim.x, blockIdx.x) + warp;
+    // One table per tensor: a grid-stride walk (the whole grid sweeps one
+    // window at a time).  Per-row / per-group scales: each CTA walks its own
+    // contiguous range, warps interleaved, so a warp's scale changes rarely.
+    constexpr bool kGrid = (SRC == Src::TENSOR);
+    const int64_t ustep = kGrid ? (int64_t)gridDim.x * kWarps : kWarps;
+    const int64_t c1 = kGrid ? a.units : split_at(a.units, gridDim.x, blockIdx.x + 1);
+    const int64_t u0 = kGrid ? (int64_t)blockIdx.x * kWarps + warp
+                             : split_at(a.units, gridDim.x, blockIdx.x) + warp;
     if (u0 >= c1) return;
+    const int64_t step_rows = ustep / a.cpr, step_chunks = ustep % a.cpr;
     constexpr int64_t kElt = (IT == In::F32) ? 4 : 2;
     const char* xb = static_cast<const char*>(a.x);
     const int t = lane & 3, r = lane >> 2;
@@ -574,15 +697,16 @@ __global__ void __launch_bounds__(kThreads, tile_min_ctas<IT>()) k_quant16x16(co
         S = global_scale(a.amax[0], a.six_bound);
         build_table(tbl, S, lane);
     }
-    for (int64_t u = u0; u < c1; u += kWarps) {
-        RowChunk nc = cc;  // this warp's next unit, kWarps units on
-        nc.chunk += kWarps;
-        while (nc.chunk >= a.cpr) {
+    for (int64_t u = u0; u < c1; u += ustep) {
+        RowChunk nc = cc;  // this warp's next unit, ustep units on
+        nc.row += step_rows;
+        nc.chunk += step_chunks;
+        if (nc.chunk >= a.cpr) {
             nc.chunk -= a.cpr;
             ++nc.row;
         }
         Raw<IT> nxt0, nxt1;
-        load_unit(nxt0, nxt1, nc, u + kWarps < c1);
+        load_unit(nxt0, nxt1, nc, u + ustep < c1);
         const int64_t band = cc.row;
         bool tail = false;
         if constexpr (SRC != Src::TENSOR) {

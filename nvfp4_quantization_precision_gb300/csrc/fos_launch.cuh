@@ -118,6 +118,7 @@ cudaError_t launch_quant16x16_f16(Err, Src, const EncArgs&, cudaStream_t);
 cudaError_t launch_quant16x16_f32(Err, Src, const EncArgs&, cudaStream_t);
 cudaError_t launch_qdq(In, Err, const QdqArgs&, cudaStream_t);
 cudaError_t launch_qdq_fused(In, Err, const QdqFusedArgs&, cudaStream_t);
+cudaError_t launch_colwise(In, Err, bool dual, const ColArgs&, cudaStream_t);
 cudaError_t launch_pipe(In, Err, const PipeArgs&, cudaStream_t);
 cudaError_t launch_dequant(Out, bool b16, Src, const DeqArgs&, cudaStream_t);
 cudaError_t launch_amax(In, Src, const AmaxArgs&, cudaStream_t);

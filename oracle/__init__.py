@@ -221,6 +221,13 @@ def quantize(x, cfg: Config, amax=None, with_errors=False):
     return codes, scales, a
 
 
+def quantize_colwise(x, cfg: Config, amax=None):
+    """The column-wise operand: the quantization of x^T (blocks of 16
+    consecutive rows of one column of x), by definition quantize(x.T).  The
+    per-tensor amax of x^T is that of x."""
+    return quantize(np.ascontiguousarray(_f32(x).T), cfg, amax=amax)
+
+
 _OUTK = {"f32": (OUT_F32, np.float32), "bf16": (OUT_BF16, np.uint16), "f16": (OUT_F16, np.uint16)}
 
 

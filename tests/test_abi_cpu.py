@@ -208,3 +208,17 @@ def test_qdq_fused_rejects_before_any_cuda_call(L):
 def test_workspace_error_rejects_null(L):
     code = ctypes.c_int(7)
     assert L.fos_workspace_error(None, None, ctypes.byref(code)) == fos.FOS_ERR_INVALID_ARG
+
+
+def test_quantize_colwise_rejects_before_any_cuda_call(L):
+    L.fos_quantize_colwise.restype = ctypes.c_int
+    c = _cfg()
+
+    def call(rows=32, cols=32, cfg=c, codes=FAKE, scales=FAKE):
+        return L.fos_quantize_colwise(FAKE, 0, ctypes.c_int64(rows), ctypes.c_int64(cols),
+                                      ctypes.byref(cfg), FAKE, FAKE, FAKE, codes, scales, None)
+    assert call(rows=24) == fos.FOS_ERR_UNSUPPORTED          # blocks of x^T run down the rows
+    assert call(cols=24) == fos.FOS_ERR_UNSUPPORTED
+    assert call(cfg=_cfg(block=1)) == fos.FOS_ERR_UNSUPPORTED
+    assert call(cfg=_cfg(granularity=1)) == fos.FOS_ERR_UNSUPPORTED
+    assert call(codes=None) == fos.FOS_ERR_INVALID_ARG        # codes and scales go together

@@ -623,3 +623,54 @@ def test_qdq_fused_equals_separate_amax_passes_full_size():
         for o, r, a, b in zip(outs, ref, amaxes, a2):
             assert torch.equal(o.view(torch.int16), r.view(torch.int16))
             assert torch.equal(a, b)
+
+
+# ------------------------------------------------------------------ column-wise operand
+@pytest.mark.parametrize("dt", ["bf16", "f16", "f32"])
+@pytest.mark.parametrize("mode", ["std", "mse", "mae_f16"])
+@pytest.mark.parametrize("dual", [False, True])
+def test_quantize_colwise(dt, mode, dual):
+    """x^T quantized from x: whole and ragged 64 x 256 tiles, amax computed
+    (first two shapes) and given; with dual the row-wise result of the same
+    read equals fos_quantize's oracle result."""
+    gcfg, ocfg = _cfgs(mode, 448)
+    for i, (shape, fam) in enumerate(zip([(64, 256), (80, 272), (16, 16), (1024, 4096),
+                                          (48, 4112)], list(workloads.FAMILIES) + ["F2"])):
+        x = _x(*shape, fam, seed=120 + i, dt=dt)
+        xf = x.float().numpy()
+        given = i >= 2
+        if given:
+            a = oracle.amax_tensor(xf)
+            ocfg2 = oracle.Config(**{**ocfg.__dict__, "amax_is_input": True})
+            oct_, ost, oa = oracle.quantize_colwise(xf, ocfg2, amax=a)
+            orc_, ors, _ = oracle.quantize(xf, ocfg2, amax=a)
+            res = fos.quantize_colwise(x.to(DEV), gcfg, amax=torch.from_numpy(a).to(DEV),
+                                       rowwise=dual)
+        else:
+            oct_, ost, oa = oracle.quantize_colwise(xf, ocfg)
+            orc_, ors, _ = oracle.quantize(xf, ocfg)
+            res = fos.quantize_colwise(x.to(DEV), gcfg, rowwise=dual)
+        torch.cuda.synchronize()
+        assert np.array_equal(_u32(res[2]), oa.view(np.uint32)), shape
+        assert np.array_equal(res[0].cpu().numpy(), oct_), shape
+        assert np.array_equal(res[1].cpu().numpy(), ost), shape
+        if dual:
+            assert np.array_equal(res[3].cpu().numpy(), orc_), shape
+            assert np.array_equal(res[4].cpu().numpy(), ors), shape
+
+
+def test_quantize_colwise_full_size_sampled():
+    """8192x4096 bf16, both layouts from one read, amax computed: the
+    row-wise result equals fos_quantize's, sampled columns equal the oracle."""
+    x = workloads.activation(8192, 4096, "F2", seed=3, device=DEV)
+    gcfg, ocfg = _cfgs("mse", 448)
+    ct, st, a, c, s_ = fos.quantize_colwise(x, gcfg, rowwise=True)
+    c1, s1, a1 = fos.quantize(x, gcfg)
+    torch.cuda.synchronize()
+    assert torch.equal(a, a1) and torch.equal(c, c1) and torch.equal(s_, s1)
+    cols = np.random.default_rng(4).choice(4096, 24, replace=False)
+    xc = x[:, torch.from_numpy(cols).to(DEV)].cpu().float().numpy()  # [8192, 24]
+    ocfg2 = oracle.Config(**{**ocfg.__dict__, "amax_is_input": True})
+    oct_, ost, _ = oracle.quantize_colwise(xc, ocfg2, amax=a.cpu().numpy())
+    assert np.array_equal(ct.cpu().numpy()[cols], oct_)
+    assert np.array_equal(st.cpu().numpy()[cols], ost)

@@ -519,3 +519,26 @@ def test_scale_order_golden(orc):
     cfg = orc.Config(four_over_six=False, amax_is_input=True, bound=448)
     _, scales, _ = orc.quantize(x, cfg, amax=[float(amax)])
     assert scales[0, 0] == int(code_hex, 16)
+
+
+# ---------------------------------------------------------------- column-wise operand
+def test_colwise_is_the_quantization_of_each_column(orc):
+    """Row c of the column-wise result equals the quantization of column c
+    of x taken on its own as one row (same global amax given), and the
+    scales follow the same blocks (16 consecutive rows)."""
+    x = workloads.activation(64, 48, "F2", seed=9, dtype=torch.float32).numpy()
+    A = orc.amax_tensor(x)
+    cfg = orc.Config(four_over_six=True, mse=True, amax_is_input=True)
+    ct, st, _ = orc.quantize_colwise(x, cfg, amax=A)
+    assert ct.shape == (48, 32) and st.shape == (48, 4)
+    for c in (0, 7, 47):
+        cc, sc, _ = orc.quantize(x[:, c].reshape(1, 64).copy(), cfg, amax=A)
+        assert np.array_equal(ct[c], cc[0]) and np.array_equal(st[c], sc[0])
+
+
+def test_colwise_of_a_symmetric_matrix_is_the_rowwise_result(orc):
+    a = workloads.activation(32, 32, "F1", seed=10, dtype=torch.float32).numpy()
+    x = (a + a.T).astype(np.float32)
+    cfg = orc.Config(four_over_six=True, mse=False, err_f16=True)
+    assert all(np.array_equal(p, q) for p, q in zip(orc.quantize_colwise(x, cfg),
+                                                      orc.quantize(x, cfg)))
