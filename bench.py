@@ -278,6 +278,14 @@ def run_fos(args):
     codes = [torch.empty(ROWS, COLS // 2, dtype=torch.uint8, device=dev) for _ in xs]
     scales = [torch.empty(ROWS, COLS // 16, dtype=torch.uint8, device=dev) for _ in xs]
     cfg = fos.Config(four_over_six=True, mse=True, err_f16=False, bound=448)
+    if args.rows_only:
+        # a subset of the per-row timings only (for profiling one kernel)
+        only = set(args.rows_only.split(","))
+        res = _rows(fos, xs, stream, peak, only)
+        torch.cuda.synchronize()
+        if rank == 0:
+            print(json.dumps({"rows": res, "sections": sorted(only)}))
+        return
 
     # One step = one fos_quantize_list call over the four tensors (per-tensor
     # amax computed): the amax pass of tensor 0, then one launch per tensor
@@ -411,9 +419,10 @@ def _e2e(fos, xs, cfg, stream, args, ws, dev):
             "steps": reps}
 
 
-def _rows(fos, xs, stream, peak):
+def _rows(fos, xs, stream, peak, only=None):
     """Device time of every hot-path row at its workload size, each from a
-    CUDA graph of 8 calls rotating over inputs larger than L2."""
+    CUDA graph of 8 calls rotating over inputs larger than L2.  `only`: the
+    sections to run (all when None)."""
     import torch
 
     import workloads
@@ -432,142 +441,156 @@ def _rows(fos, xs, stream, peak):
         res[name] = {"GB/s": round(nbytes / (ms / 1e3) / 1e9, 1), "us": round(ms * 1e3, 2),
                      "frac": round(nbytes / (ms / 1e3) / 1e9 / peak, 3)}
 
-    # a1: amax pass (reads x once)
-    tmp = torch.zeros(1, dtype=torch.float32, device=dev)
-    rec("amax_pass", ELEMS * 2, _graph_ms(rot(lambda i: fos.amax(xs[i], out=tmp)), R8, stream))
-    # a2-a8: encode sweep, amax given
+    def want(section):
+        return only is None or section in only
+
     codes = torch.empty(ROWS, COLS // 2, dtype=torch.uint8, device=dev)
     scales = torch.empty(ROWS, COLS // 16, dtype=torch.uint8, device=dev)
-    sweep = {}
-    for four, mse, f16, bound, row in (
-            [(False, True, False, 448, False), (False, True, False, 448, True)] +
-            [(True, m, h, b, r) for m in (False, True) for h in (False, True)
-             for b in (448, 256) for r in (False, True)]):
-        c = fos.Config(four_over_six=four, mse=mse, err_f16=f16, bound=bound, row_scaled=row)
-        a = ra if row else am
-        ms = _graph_ms(rot(lambda i: fos.quantize(xs[i], c, amax=a[i], codes=codes,
-                                                  scales=scales)), R8, stream)
-        name = ("std" if not four else ("mse" if mse else "mae") + ("_f16" if f16 else "_exact")
-                ) + "_%d_%s" % (bound, "row" if row else "tensor")
-        sweep[name] = round(ALG_BYTES / (ms / 1e3) / 1e9, 1)
-    for mse in (False, True):  # the sequential error-term order, per-tensor scale
-        c = fos.Config(mse=mse, err_f16=True, seq_order=True)
-        ms = _graph_ms(rot(lambda i: fos.quantize(xs[i], c, amax=am[i], codes=codes,
-                                                  scales=scales)), R8, stream)
-        sweep[("mse" if mse else "mae") + "_f16_448_tensor_seq"] = round(
-            ALG_BYTES / (ms / 1e3) / 1e9, 1)
-    res["encode_sweep_GB/s"] = sweep
-    # a1+a8 with the row amax fused?  (row amax is a separate pass; both timed)
-    ms = _graph_ms(rot(lambda i: fos.quantize(xs[i], fos.Config(row_scaled=True),
-                                              codes=codes, scales=scales)), R8, stream)
-    rec("encode_row_scaled_with_amax_pass", ALG_BYTES, ms)
-    # the column-wise operand (x^T) alone and with the row-wise result of
-    # the same read, 4/6 MSE, amax given
-    ct = torch.empty(COLS, ROWS // 2, dtype=torch.uint8, device=dev)
-    st_ = torch.empty(COLS, ROWS // 16, dtype=torch.uint8, device=dev)
-    c = fos.Config()
-    ms = _graph_ms(rot(lambda i: fos.quantize_colwise(xs[i], c, amax=am[i], codes_t=ct,
-                                                      scales_t=st_)), R8, stream)
-    rec("colwise_8192x4096_bf16_mse", ALG_BYTES, ms)
-    ms = _graph_ms(rot(lambda i: fos.quantize_colwise(xs[i], c, amax=am[i], codes_t=ct,
-                                                      scales_t=st_, codes=codes, scales=scales)),
-                   R8, stream)
-    rec("colwise_and_rowwise_8192x4096_bf16_mse", ELEMS * (2 + 2 * (0.5 + 1 / 16)), ms)
-    del ct, st_
-    # a9: fused QDQ at the metric shape and on the 8 x 2048x7168 weight list
-    outs4 = [torch.empty_like(x) for x in xs]
-    for mode in ("std", "mse_f16", "mse_exact"):
-        c = fos.Config(four_over_six=(mode != "std"), mse=True, err_f16=(mode == "mse_f16"))
-        ms = _graph_ms(rot(lambda i: fos.qdq([xs[i]], c, amaxes=[am[i]], outs=[outs4[i]])),
+
+    if want("amax"):
+        # a1: amax pass (reads x once)
+        tmp = torch.zeros(1, dtype=torch.float32, device=dev)
+        rec("amax_pass", ELEMS * 2, _graph_ms(rot(lambda i: fos.amax(xs[i], out=tmp)), R8, stream))
+    if want("encode"):
+        # a2-a8: encode sweep, amax given
+        sweep = {}
+        for four, mse, f16, bound, row in (
+                [(False, True, False, 448, False), (False, True, False, 448, True)] +
+                [(True, m, h, b, r) for m in (False, True) for h in (False, True)
+                 for b in (448, 256) for r in (False, True)]):
+            c = fos.Config(four_over_six=four, mse=mse, err_f16=f16, bound=bound, row_scaled=row)
+            a = ra if row else am
+            ms = _graph_ms(rot(lambda i: fos.quantize(xs[i], c, amax=a[i], codes=codes,
+                                                      scales=scales)), R8, stream)
+            name = ("std" if not four else ("mse" if mse else "mae") + ("_f16" if f16 else "_exact")
+                    ) + "_%d_%s" % (bound, "row" if row else "tensor")
+            sweep[name] = round(ALG_BYTES / (ms / 1e3) / 1e9, 1)
+        for mse in (False, True):  # the sequential error-term order, per-tensor scale
+            c = fos.Config(mse=mse, err_f16=True, seq_order=True)
+            ms = _graph_ms(rot(lambda i: fos.quantize(xs[i], c, amax=am[i], codes=codes,
+                                                      scales=scales)), R8, stream)
+            sweep[("mse" if mse else "mae") + "_f16_448_tensor_seq"] = round(
+                ALG_BYTES / (ms / 1e3) / 1e9, 1)
+        res["encode_sweep_GB/s"] = sweep
+        # a1+a8 with the row amax fused?  (row amax is a separate pass; both timed)
+        ms = _graph_ms(rot(lambda i: fos.quantize(xs[i], fos.Config(row_scaled=True),
+                                                  codes=codes, scales=scales)), R8, stream)
+        rec("encode_row_scaled_with_amax_pass", ALG_BYTES, ms)
+    if want("colwise"):
+        # the column-wise operand (x^T) alone and with the row-wise result of
+        # the same read, 4/6 MSE, amax given
+        ct = torch.empty(COLS, ROWS // 2, dtype=torch.uint8, device=dev)
+        st_ = torch.empty(COLS, ROWS // 16, dtype=torch.uint8, device=dev)
+        c = fos.Config()
+        ms = _graph_ms(rot(lambda i: fos.quantize_colwise(xs[i], c, amax=am[i], codes_t=ct,
+                                                          scales_t=st_)), R8, stream)
+        rec("colwise_8192x4096_bf16_mse", ALG_BYTES, ms)
+        ms = _graph_ms(rot(lambda i: fos.quantize_colwise(xs[i], c, amax=am[i], codes_t=ct,
+                                                          scales_t=st_, codes=codes, scales=scales)),
                        R8, stream)
-        rec("qdq_8192x4096_bf16_" + mode, ELEMS * 4, ms)
-    del outs4
-    ws_ = workloads.qdq_weights(8, 2048, 7168, seed=0, device=dev)
-    wam = [fos.amax(t) for t in ws_]
-    wout = [torch.empty_like(t) for t in ws_]
-    for mode in ("std", "mse_f16", "mae_f16", "mse_f16_seq", "mae_f16_seq"):
-        c = fos.Config(four_over_six=(mode != "std"), mse=not mode.startswith("mae"),
-                       err_f16=True, seq_order=mode.endswith("_seq"))
-        ms = _graph_ms(lambda: fos.qdq(ws_, c, amaxes=wam, outs=wout), 2, stream)
-        rec("qdq_list_8x2048x7168_bf16_" + mode, sum(t.numel() for t in ws_) * 4, ms)
-    # the same list with the per-tensor amax computed: separate amax passes
-    # then the QDQ launch, against one fused persistent launch (the bytes
-    # counted are the QDQ's, 4 per element, as above: strict)
-    c = fos.Config(err_f16=True, seq_order=True)
-    wsp = fos.qdq_fused_workspace(len(ws_), dev)
-    ms = _graph_ms(lambda: fos.qdq(ws_, c, amaxes=wam, outs=wout, amax_given=False), 2, stream)
-    rec("qdq_list_8x2048x7168_bf16_mse_f16_seq_amax_separate", sum(t.numel() for t in ws_) * 4,
-        ms)
-    ms = _graph_ms(lambda: fos.qdq_fused(ws_, c, amaxes=wam, outs=wout, workspace=wsp), 2,
-                   stream)
-    rec("qdq_list_8x2048x7168_bf16_mse_f16_seq_amax_fused", sum(t.numel() for t in ws_) * 4, ms)
-    if fos.workspace_error(wsp) != 0:
-        raise RuntimeError("fused QDQ: a wait between warps ran out")
-    del ws_, wout
-    # the Megatron page's own benchmark shape: eight 4096x6144 bf16 weights,
-    # fused QDQ with the caller's amax and the sequential (TE) term order
-    ws_ = workloads.qdq_weights(8, 4096, 6144, seed=1, device=dev)
-    wam = [fos.amax(t) for t in ws_]
-    wout = [torch.empty_like(t) for t in ws_]
-    for mode in ("std", "mae_f16_seq", "mse_f16_seq"):
-        c = fos.Config(four_over_six=(mode != "std"), mse=not mode.startswith("mae"),
-                       err_f16=True, seq_order=mode.endswith("_seq"))
-        ms = _graph_ms(lambda: fos.qdq(ws_, c, amaxes=wam, outs=wout), 2, stream)
-        rec("qdq_list_8x4096x6144_bf16_" + mode, sum(t.numel() for t in ws_) * 4, ms)
-    del ws_, wout
-    # a11: dequantize back to bf16
-    c = fos.Config()
-    cs = [fos.quantize(x, c, amax=a) for x, a in zip(xs, am)]
-    out = torch.empty(ROWS, COLS, dtype=torch.bfloat16, device=dev)
-    ms = _graph_ms(rot(lambda i: fos.dequantize(cs[i][0], cs[i][1], am[i], c, out=out)), R8,
-                   stream)
-    rec("dequantize_bf16", ALG_BYTES, ms)
-    del cs
-    # a10: grouped MoE activations, 65536 x 7168 in 64 groups, per-group amax
-    R, C = 65536, 7168
-    offs = workloads.moe_offsets(R, 64, seed=0)
-    xa = workloads.moe_activations(R, C, offs, seed=0, device=dev)
-    offs = offs.to(dev)
-    ga = torch.empty(64, dtype=torch.float32, device=dev)
-    gc = torch.empty(R, C // 2, dtype=torch.uint8, device=dev)
-    gs = torch.empty(R, C // 16, dtype=torch.uint8, device=dev)
-    c = fos.Config()
-    fos.quantize_grouped(xa, offs, c, group_amax=ga, codes=gc, scales=gs)
-    live = int(offs[-1].item())
-    gbytes = live * C * BYTES_PER_ELEM + (R - live) * C * (0.5 + 1 / 16)
-    ms = _graph_ms(lambda: fos.quantize_grouped(xa, offs, c, group_amax=ga, codes=gc, scales=gs),
-                   2, stream)
-    rec("grouped_moe_65536x7168_amax_given", gbytes, ms)
-    del xa, gc, gs
-    # 16x16 weight quantize 14336 x 4096 bf16 (and fp32)
-    for dt in (torch.bfloat16, torch.float32):
-        w = workloads.weight(14336, 4096, seed=0, dtype=dt, device=dev)
-        wa = fos.amax(w)
-        c = fos.Config(block16x16=True)
-        wc = torch.empty(14336, 2048, dtype=torch.uint8, device=dev)
-        wsc = torch.empty(896, 256, dtype=torch.uint8, device=dev)
-        ms = _graph_ms(lambda: fos.quantize(w, c, amax=wa, codes=wc, scales=wsc), 4, stream)
-        esz = 2 if dt == torch.bfloat16 else 4
-        rec("weight_16x16_14336x4096_" + ("bf16" if esz == 2 else "fp32"),
-            14336 * 4096 * (esz + 0.5 + 1 / 256), ms)
-        if dt == torch.bfloat16:
-            wo = torch.empty(14336, 4096, dtype=torch.bfloat16, device=dev)
-            ms = _graph_ms(lambda: fos.dequantize(wc, wsc, wa, c, out=wo), 4, stream)
-            rec("weight_16x16_dequantize_bf16", 14336 * 4096 * (0.5 + 1 / 256 + 2), ms)
-            del wo
-        del w
-    # expert stack 64 x 2048x7168 bf16, 16x16 tiles, one flattened call with
-    # each expert's amax expanded to its rows
-    E, ER, EC = 64, 2048, 7168
-    xe = workloads.moe_experts(E, ER, EC, seed=0, device=dev).view(E * ER, EC)
-    ea = torch.stack([fos.amax(xe[e * ER:(e + 1) * ER])[0] for e in range(E)])
-    ra_e = ea.repeat_interleave(ER)
-    c = fos.Config(block16x16=True, row_scaled=True)
-    ec = torch.empty(E * ER, EC // 2, dtype=torch.uint8, device=dev)
-    es = torch.empty(E * ER // 16, EC // 16, dtype=torch.uint8, device=dev)
-    ms = _graph_ms(lambda: fos.quantize(xe, c, amax=ra_e, codes=ec, scales=es), 2, stream)
-    rec("experts_16x16_64x2048x7168_bf16", E * ER * EC * (2 + 0.5 + 1 / 256), ms)
-    del xe, ec, es
+        rec("colwise_and_rowwise_8192x4096_bf16_mse", ELEMS * (2 + 2 * (0.5 + 1 / 16)), ms)
+        del ct, st_
+    if want("qdq"):
+        # a9: fused QDQ at the metric shape
+        outs4 = [torch.empty_like(x) for x in xs]
+        for mode in ("std", "mse_f16", "mse_exact"):
+            c = fos.Config(four_over_six=(mode != "std"), mse=True, err_f16=(mode == "mse_f16"))
+            ms = _graph_ms(rot(lambda i: fos.qdq([xs[i]], c, amaxes=[am[i]], outs=[outs4[i]])),
+                           R8, stream)
+            rec("qdq_8192x4096_bf16_" + mode, ELEMS * 4, ms)
+        del outs4
+    if want("qdq_list"):
+        ws_ = workloads.qdq_weights(8, 2048, 7168, seed=0, device=dev)
+        wam = [fos.amax(t) for t in ws_]
+        wout = [torch.empty_like(t) for t in ws_]
+        for mode in ("std", "mse_f16", "mae_f16", "mse_f16_seq", "mae_f16_seq"):
+            c = fos.Config(four_over_six=(mode != "std"), mse=not mode.startswith("mae"),
+                           err_f16=True, seq_order=mode.endswith("_seq"))
+            ms = _graph_ms(lambda: fos.qdq(ws_, c, amaxes=wam, outs=wout), 2, stream)
+            rec("qdq_list_8x2048x7168_bf16_" + mode, sum(t.numel() for t in ws_) * 4, ms)
+        # the same list with the per-tensor amax computed: separate amax passes
+        # then the QDQ launch, against one fused persistent launch (the bytes
+        # counted are the QDQ's, 4 per element, as above: strict)
+        c = fos.Config(err_f16=True, seq_order=True)
+        wsp = fos.qdq_fused_workspace(len(ws_), dev)
+        ms = _graph_ms(lambda: fos.qdq(ws_, c, amaxes=wam, outs=wout, amax_given=False), 2, stream)
+        rec("qdq_list_8x2048x7168_bf16_mse_f16_seq_amax_separate", sum(t.numel() for t in ws_) * 4,
+            ms)
+        ms = _graph_ms(lambda: fos.qdq_fused(ws_, c, amaxes=wam, outs=wout, workspace=wsp), 2,
+                       stream)
+        rec("qdq_list_8x2048x7168_bf16_mse_f16_seq_amax_fused", sum(t.numel() for t in ws_) * 4, ms)
+        if fos.workspace_error(wsp) != 0:
+            raise RuntimeError("fused QDQ: a wait between warps ran out")
+        del ws_, wout
+    if want("qdq_page"):
+        # the Megatron page's own benchmark shape: eight 4096x6144 bf16 weights,
+        # fused QDQ with the caller's amax and the sequential (TE) term order
+        ws_ = workloads.qdq_weights(8, 4096, 6144, seed=1, device=dev)
+        wam = [fos.amax(t) for t in ws_]
+        wout = [torch.empty_like(t) for t in ws_]
+        for mode in ("std", "mae_f16_seq", "mse_f16_seq"):
+            c = fos.Config(four_over_six=(mode != "std"), mse=not mode.startswith("mae"),
+                           err_f16=True, seq_order=mode.endswith("_seq"))
+            ms = _graph_ms(lambda: fos.qdq(ws_, c, amaxes=wam, outs=wout), 2, stream)
+            rec("qdq_list_8x4096x6144_bf16_" + mode, sum(t.numel() for t in ws_) * 4, ms)
+        del ws_, wout
+    if want("dequant"):
+        # a11: dequantize back to bf16
+        c = fos.Config()
+        cs = [fos.quantize(x, c, amax=a) for x, a in zip(xs, am)]
+        out = torch.empty(ROWS, COLS, dtype=torch.bfloat16, device=dev)
+        ms = _graph_ms(rot(lambda i: fos.dequantize(cs[i][0], cs[i][1], am[i], c, out=out)), R8,
+                       stream)
+        rec("dequantize_bf16", ALG_BYTES, ms)
+        del cs
+    if want("grouped"):
+        # a10: grouped MoE activations, 65536 x 7168 in 64 groups, per-group amax
+        R, C = 65536, 7168
+        offs = workloads.moe_offsets(R, 64, seed=0)
+        xa = workloads.moe_activations(R, C, offs, seed=0, device=dev)
+        offs = offs.to(dev)
+        ga = torch.empty(64, dtype=torch.float32, device=dev)
+        gc = torch.empty(R, C // 2, dtype=torch.uint8, device=dev)
+        gs = torch.empty(R, C // 16, dtype=torch.uint8, device=dev)
+        c = fos.Config()
+        fos.quantize_grouped(xa, offs, c, group_amax=ga, codes=gc, scales=gs)
+        live = int(offs[-1].item())
+        gbytes = live * C * BYTES_PER_ELEM + (R - live) * C * (0.5 + 1 / 16)
+        ms = _graph_ms(lambda: fos.quantize_grouped(xa, offs, c, group_amax=ga, codes=gc, scales=gs),
+                       2, stream)
+        rec("grouped_moe_65536x7168_amax_given", gbytes, ms)
+        del xa, gc, gs
+    if want("weight"):
+        # 16x16 weight quantize 14336 x 4096 bf16 (and fp32)
+        for dt in (torch.bfloat16, torch.float32):
+            w = workloads.weight(14336, 4096, seed=0, dtype=dt, device=dev)
+            wa = fos.amax(w)
+            c = fos.Config(block16x16=True)
+            wc = torch.empty(14336, 2048, dtype=torch.uint8, device=dev)
+            wsc = torch.empty(896, 256, dtype=torch.uint8, device=dev)
+            ms = _graph_ms(lambda: fos.quantize(w, c, amax=wa, codes=wc, scales=wsc), 4, stream)
+            esz = 2 if dt == torch.bfloat16 else 4
+            rec("weight_16x16_14336x4096_" + ("bf16" if esz == 2 else "fp32"),
+                14336 * 4096 * (esz + 0.5 + 1 / 256), ms)
+            if dt == torch.bfloat16:
+                wo = torch.empty(14336, 4096, dtype=torch.bfloat16, device=dev)
+                ms = _graph_ms(lambda: fos.dequantize(wc, wsc, wa, c, out=wo), 4, stream)
+                rec("weight_16x16_dequantize_bf16", 14336 * 4096 * (0.5 + 1 / 256 + 2), ms)
+                del wo
+            del w
+    if want("experts"):
+        # expert stack 64 x 2048x7168 bf16, 16x16 tiles, one flattened call with
+        # each expert's amax expanded to its rows
+        E, ER, EC = 64, 2048, 7168
+        xe = workloads.moe_experts(E, ER, EC, seed=0, device=dev).view(E * ER, EC)
+        ea = torch.stack([fos.amax(xe[e * ER:(e + 1) * ER])[0] for e in range(E)])
+        ra_e = ea.repeat_interleave(ER)
+        c = fos.Config(block16x16=True, row_scaled=True)
+        ec = torch.empty(E * ER, EC // 2, dtype=torch.uint8, device=dev)
+        es = torch.empty(E * ER // 16, EC // 16, dtype=torch.uint8, device=dev)
+        ms = _graph_ms(lambda: fos.quantize(xe, c, amax=ra_e, codes=ec, scales=es), 2, stream)
+        rec("experts_16x16_64x2048x7168_bf16", E * ER * EC * (2 + 0.5 + 1 / 256), ms)
+        del xe, ec, es
     return res
 
 
@@ -621,6 +644,9 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--skip-extras", action="store_true",
                     help="only the timed step (no e2e / per-row / CPU baseline)")
+    ap.add_argument("--rows-only", default="",
+                    help="comma list of row sections to time alone (amax, encode, colwise, qdq, "
+                         "qdq_list, qdq_page, dequant, grouped, weight, experts); no step")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
