@@ -6,7 +6,7 @@ namespace fos {
 
 template <In IT, Err EM>
 static cudaError_t go(bool dual, const ColArgs& a, cudaStream_t s) {
-    constexpr size_t kSmem = (size_t)kColTileR * kColTileC * (IT == In::F32 ? 4 : 2);
+    constexpr size_t kSmem = 2 * (size_t)ColTile<IT>::kBytes + 128;  // two tiles, aligned
     const int64_t units = a.tiles * kWarps;  // one CTA per tile at most
     if (dual) return launch_persistent(k_quant_colwise<IT, EM, true>, a, units, kSmem, s);
     return launch_persistent(k_quant_colwise<IT, EM, false>, a, units, kSmem, s);

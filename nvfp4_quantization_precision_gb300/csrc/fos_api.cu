@@ -8,7 +8,10 @@
 // the host.
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 #include <vector>
+
+#include <cudaTypedefs.h>
 
 #include "../../include/fos.h"
 #include "../../include/fos_diag.h"
@@ -304,6 +307,39 @@ fos_status check_quant_args(const void* x, int64_t rows, int64_t cols, const fos
     if (!x || !amax || !codes || !scales) return FOS_ERR_INVALID_ARG;
     if (!aligned(x, 32) || !aligned(codes, 8)) return FOS_ERR_MISALIGNED;
     return FOS_OK;
+}
+
+// 2D TMA descriptor of x [rows, cols] with the column-wise tile as its box.
+// cuTensorMapEncodeTiled is a driver function; its address comes from the
+// runtime once (no link against the driver library).
+fos_status encode_tile_map(CUtensorMap* map, const void* x, fos_dtype dt, int64_t rows,
+                           int64_t cols) {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+        else
+            cudaGetLastError();
+    });
+    if (!fn) return FOS_ERR_CUDA;
+    const bool f32 = dt == FOS_FP32;
+    const CUtensorMapDataType ty = f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                       : (dt == FOS_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                         : CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)cols * (f32 ? 4 : 2)};
+    const cuuint32_t box[2] = {(cuuint32_t)ColTile<In::BF16>::kC,
+                               (cuuint32_t)(f32 ? ColTile<In::F32>::kR : ColTile<In::BF16>::kR)};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = fn(map, ty, 2, const_cast<void*>(x), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? FOS_OK : FOS_ERR_CUDA;
 }
 
 // One quantize on the current device (arguments already validated).
@@ -729,6 +765,8 @@ fos_status fos_quantize_colwise(const void* x, fos_dtype dt, int64_t rows, int64
     if (!x || !codes_t || !scales_t) return FOS_ERR_INVALID_ARG;
     if (!aligned(x, 32) || !aligned(codes_t, 8) || (dual && !aligned(codes, 8)))
         return FOS_ERR_MISALIGNED;
+    if (rows >= (INT64_C(1) << 31) || cols >= (INT64_C(1) << 31))  // tile coordinates are int32
+        return FOS_ERR_UNSUPPORTED;
     const int dev = dual ? common_device({x, amax, codes_t, scales_t, codes, scales})
                          : common_device({x, amax, codes_t, scales_t});
     if (dev < 0) return FOS_ERR_INVALID_ARG;
@@ -740,7 +778,8 @@ fos_status fos_quantize_colwise(const void* x, fos_dtype dt, int64_t rows, int64
         if (st) return st;
     }
     ColArgs a{};
-    a.x = x;
+    st = encode_tile_map(&a.tmap, x, dt, rows, cols);
+    if (st) return st;
     a.codes_t = codes_t;
     a.scales_t = scales_t;
     a.codes = codes;
@@ -748,8 +787,10 @@ fos_status fos_quantize_colwise(const void* x, fos_dtype dt, int64_t rows, int64
     a.amax = amax;
     a.rows = rows;
     a.cols = cols;
-    a.tiles_c = (cols + kColTileC - 1) / kColTileC;
-    a.tiles = ((rows + kColTileR - 1) / kColTileR) * a.tiles_c;
+    const int tile_r = (dt == FOS_FP32) ? ColTile<In::F32>::kR : ColTile<In::BF16>::kR;
+    const int tile_c = ColTile<In::BF16>::kC;
+    a.tiles_c = (cols + tile_c - 1) / tile_c;
+    a.tiles = ((rows + tile_r - 1) / tile_r) * a.tiles_c;
     a.six_bound = 6.0f * (float)cfg->e4m3_bound;
     a.neg_zero = -0.0f;
     return cuda_status(launch_colwise(in_of(dt), err_of(cfg), dual, a, s));

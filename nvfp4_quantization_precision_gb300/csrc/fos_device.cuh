@@ -230,6 +230,16 @@ __device__ __forceinline__ void st256(void* p, const uint32_t* w) {
                  "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
                  : "memory");
 }
+__device__ __forceinline__ void st128(void* p, const uint32_t* w) {
+    asm volatile("st.global.v4.b32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(w[0]), "r"(w[1]),
+                 "r"(w[2]), "r"(w[3]) : "memory");
+}
+__device__ __forceinline__ void st32(void* p, uint32_t a) {
+    asm volatile("st.global.b32 [%0], %1;" ::"l"(p), "r"(a) : "memory");
+}
+__device__ __forceinline__ void st16(void* p, uint32_t a) {
+    asm volatile("st.global.b16 [%0], %1;" ::"l"(p), "h"((unsigned short)a) : "memory");
+}
 __device__ __forceinline__ void st64(void* p, uint32_t a, uint32_t b) {
     asm volatile("st.global.v2.b32 [%0], {%1,%2};" ::"l"(p), "r"(a), "r"(b) : "memory");
 }

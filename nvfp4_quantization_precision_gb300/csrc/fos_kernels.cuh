@@ -16,6 +16,8 @@
 // unit's input is loaded before the current one is encoded.
 #pragma once
 
+#include <cuda.h>
+
 #include "fos_device.cuh"
 
 namespace fos {
@@ -372,18 +374,29 @@ __global__ void __launch_bounds__(kThreads, min_ctas<EM>()) k_qdq1x16(const __gr
 // ------------------------------------------------------------------------
 // Column-wise quantize: the 1x16 quantization of x^T, computed from the
 // row-major x without forming x^T (the operand layout a weight-gradient
-// GEMM reads).  A CTA stages a tile of 64 rows x 256 columns in shared
-// memory: each thread loads four 16-element row segments (and, with DUAL,
-// encodes them row-wise straight from registers, so one read of x gives
-// both layouts).  Then thread c encodes the four 16-row blocks of tile
-// column c and writes 32 consecutive code bytes and 4 scale bytes of row c
-// of x^T.  Tiles are walked grid-stride; the scale is per tensor (x and x^T
-// have one amax).
+// GEMM reads).  Each CTA walks tiles of kR rows x 256 columns grid-stride.
+// A tile arrives in shared memory by one 2D TMA load (cp.async.bulk.tensor,
+// completion on an mbarrier; elements past the tensor edge are filled with
+// zeros) into one of two buffers, the next tile's load being issued before
+// the current tile is worked on.  With DUAL, each thread first encodes four
+// (two for fp32) 16-element row segments of the tile row-wise, so one read
+// of x gives both layouts.  Then thread c encodes the kR/16 16-row blocks
+// of tile column c and writes that part of row c of x^T.  The scale is per
+// tensor (x and x^T have one amax).  The mbarrier waits are bounded: a wait
+// that runs out sets the first scale byte of x^T to 0xFF (a code the
+// quantizer never writes) after draining its own load, and ends the CTA.
 // ------------------------------------------------------------------------
-constexpr int kColTileR = 64, kColTileC = 256;
+template <In IT>
+struct ColTile {
+    static constexpr int kR = (IT == In::F32) ? 32 : 64;  // tile rows
+    static constexpr int kC = 256;                         // tile columns, one per thread
+    static constexpr int kElt = (IT == In::F32) ? 4 : 2;
+    static constexpr int kBytes = kR * kC * kElt;          // 32 KiB
+};
+constexpr uint32_t kMbarSpins = 1u << 22;
 
 struct ColArgs {
-    const void* x;
+    CUtensorMap tmap;   // x as [rows, cols], box kR x 256 (2D TMA)
     uint8_t* codes_t;   // [cols, rows / 2]
     uint8_t* scales_t;  // [cols, rows / 16]
     uint8_t* codes;     // DUAL: [rows, cols / 2]
@@ -396,91 +409,185 @@ struct ColArgs {
     float neg_zero;
 };
 
-template <In IT>
-__device__ __forceinline__ void store_seg_smem(unsigned char* p, const Raw<IT>& r) {
-    uint4* q = reinterpret_cast<uint4*>(p);
-#pragma unroll
-    for (int i = 0; i < InTraits<IT>::kWords / 4; ++i)
-        q[i] = make_uint4(r.w[4 * i], r.w[4 * i + 1], r.w[4 * i + 2], r.w[4 * i + 3]);
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes) : "memory");
+}
+// Bounded wait for the phase with the given parity to complete.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+    for (uint32_t i = 0; i < kMbarSpins; ++i) {
+        uint32_t done;
+        asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                     "selp.u32 %0, 1, 0, p;\n\t}"
+                     : "=r"(done) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+        if (done) return true;
+    }
+    return false;
+}
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int32_t x, int32_t y,
+                                            uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3}], [%4];"
+        ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y),
+          "r"(smem_u32(bar)) : "memory");
 }
 
-// Elements (rb*16 .. rb*16+15, column c) of the staged tile as one segment.
+// Elements (rb*16 .. rb*16+15, column c) of a staged tile as one segment.
 template <In IT>
 __device__ __forceinline__ void gather_col(const unsigned char* tile, int rb, int c, Raw<IT>& r) {
+    constexpr int kC = ColTile<IT>::kC;
     if constexpr (IT == In::F32) {
         const uint32_t* t = reinterpret_cast<const uint32_t*>(tile);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) r.w[i] = t[(rb * 16 + i) * kColTileC + c];
+        for (int i = 0; i < 16; ++i) r.w[i] = t[(rb * 16 + i) * kC + c];
     } else {
         const uint16_t* t = reinterpret_cast<const uint16_t*>(tile);
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-            const uint32_t lo = t[(rb * 16 + 2 * j) * kColTileC + c];
-            const uint32_t hi = t[(rb * 16 + 2 * j + 1) * kColTileC + c];
+            const uint32_t lo = t[(rb * 16 + 2 * j) * kC + c];
+            const uint32_t hi = t[(rb * 16 + 2 * j + 1) * kC + c];
             r.w[j] = lo | (hi << 16);
         }
     }
 }
 
+template <In IT>
+__device__ __forceinline__ void read_seg_smem(const unsigned char* p, Raw<IT>& r) {
+    const uint4* q = reinterpret_cast<const uint4*>(p);
+#pragma unroll
+    for (int i = 0; i < InTraits<IT>::kWords / 4; ++i) {
+        const uint4 v = q[i];
+        r.w[4 * i] = v.x;
+        r.w[4 * i + 1] = v.y;
+        r.w[4 * i + 2] = v.z;
+        r.w[4 * i + 3] = v.w;
+    }
+}
+
 template <In IT, Err EM, bool DUAL>
-__global__ void __launch_bounds__(kThreads, min_ctas<EM>()) k_quant_colwise(const ColArgs a) {
+__global__ void __launch_bounds__(kThreads, min_ctas<EM>())
+    k_quant_colwise(const __grid_constant__ ColArgs a) {
+    using T = ColTile<IT>;
     chain_wait();
     chain_release();
-    constexpr int64_t kElt = (IT == In::F32) ? 4 : 2;
-    extern __shared__ __align__(16) unsigned char s_tile[];  // kColTileR x kColTileC elements
+    extern __shared__ __align__(128) unsigned char s_dyn[];  // two tiles of T::kBytes + 128
+    // TMA destinations start on 128-byte boundaries: round the base up (the
+    // launch reserves 128 spare bytes for this)
+    unsigned char* s_buf = s_dyn + ((128u - (smem_u32(s_dyn) & 127u)) & 127u);
+    __shared__ __align__(8) uint64_t s_bar[2];
     __shared__ float2 s_tbl[kWarps][128];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     float2* tbl = s_tbl[warp];
     const uint64_t nz = pk(a.neg_zero, a.neg_zero);
     const float S = global_scale(a.amax[0], a.six_bound);
     build_table(tbl, S, lane);
-    const char* xb = static_cast<const char*>(a.x);
+    if (tid == 0) {
+        mbar_init(&s_bar[0], 1);
+        mbar_init(&s_bar[1], 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    auto issue = [&](int64_t t, int b) {  // thread 0 only
+        const int32_t r0 = (int32_t)((t / a.tiles_c) * T::kR);
+        const int32_t c0 = (int32_t)((t % a.tiles_c) * T::kC);
+        mbar_expect_tx(&s_bar[b], (uint32_t)T::kBytes);
+        tma_load_2d(s_buf + b * T::kBytes, &a.tmap, c0, r0, &s_bar[b]);
+    };
+    if (tid == 0 && (int64_t)blockIdx.x < a.tiles) issue(blockIdx.x, 0);
     const int64_t nb_t = a.rows / 16;  // blocks per row of x^T
+    // wide stores of a column's codes and scales need the row count to be a
+    // multiple of the tile height and the output bases aligned to their size
+    constexpr int kNBt = T::kR / 16;
+    const bool full_rows = a.rows % T::kR == 0 &&
+                           (reinterpret_cast<uintptr_t>(a.codes_t) % (8 * kNBt)) == 0 &&
+                           (reinterpret_cast<uintptr_t>(a.scales_t) % kNBt) == 0;
     uint32_t dummy[8];
-    for (int64_t tile = blockIdx.x; tile < a.tiles; tile += gridDim.x) {
-        const int64_t r0 = (tile / a.tiles_c) * kColTileR, c0 = (tile % a.tiles_c) * kColTileC;
+    int i = 0;
+    for (int64_t tile = blockIdx.x; tile < a.tiles; tile += gridDim.x, ++i) {
+        const int b = i & 1;
+        const bool next = tile + gridDim.x < a.tiles;
+        if (tid == 0 && next) {
+            // buffer b^1 was last read in the previous tile, before the barrier
+            // that ended it; order those reads before the asynchronous write
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            issue(tile + gridDim.x, b ^ 1);
+        }
+        const bool ok = mbar_wait(&s_bar[b], (uint32_t)((i >> 1) & 1));
+        if (__syncthreads_or(!ok)) {
+            if (tid == 0) {
+                if (next) mbar_wait(&s_bar[b ^ 1], (uint32_t)(((i + 1) >> 1) & 1));  // drain
+                a.scales_t[0] = 0xFF;
+            }
+            return;
+        }
+        const unsigned char* tb = s_buf + b * T::kBytes;
+        const int64_t r0 = (tile / a.tiles_c) * T::kR, c0 = (tile % a.tiles_c) * T::kC;
+        if constexpr (DUAL) {
 #pragma unroll
-        for (int k = 0; k < (kColTileR * kColTileC / 16) / kThreads; ++k) {
-            const int seg = tid + kThreads * k;
-            const int tr = seg >> 4, ts = seg & 15;  // tile row, 16-column segment
-            const int64_t row = r0 + tr, col = c0 + ts * 16;
-            const bool v = row < a.rows && col < a.cols;
-            Raw<IT> raw;
-            zero_seg<IT>(raw);
-            if (v) load_seg<IT, kEncHint>(raw, xb + (row * a.cols + col) * kElt);
-            store_seg_smem<IT>(s_tile + ((int64_t)tr * kColTileC + ts * 16) * kElt, raw);
-            if constexpr (DUAL) {
-                if (v) {
+            for (int k = 0; k < T::kR * T::kC / 16 / kThreads; ++k) {
+                const int seg = tid + kThreads * k;
+                const int tr = seg >> 4, ts = seg & 15;  // tile row, 16-column segment
+                const int64_t row = r0 + tr, col = c0 + ts * 16;
+                if (row < a.rows && col < a.cols) {
+                    Raw<IT> raw;
+                    read_seg_smem<IT>(tb + (tr * T::kC + ts * 16) * T::kElt, raw);
                     uint64_t xp[8];
                     widen<IT>(raw, xp);
                     uint32_t code[2], scale;
                     encode_block<EM, Out::NONE>(xp, S, tbl, nz, code, scale, dummy);
-                    const int64_t b = row * (a.cols / 16) + col / 16;
-                    st64(a.codes + b * 8, code[0], code[1]);
-                    st8(a.scales + b, scale);
+                    const int64_t blk = row * (a.cols / 16) + col / 16;
+                    st64(a.codes + blk * 8, code[0], code[1]);
+                    st8(a.scales + blk, scale);
                 }
             }
         }
-        __syncthreads();
         const int64_t col = c0 + tid;  // one tile column per thread
         if (col < a.cols) {
+            constexpr int kNB = T::kR / 16;  // blocks of the column in this tile
+            // whole tile and rows a multiple of the tile height: the kNB
+            // blocks' codes (8 * kNB bytes) and scales (kNB bytes) of row col
+            // of x^T are contiguous and aligned, one store each
+            const bool whole = full_rows && r0 + T::kR <= a.rows;
+            uint32_t cw[2 * kNB], sw = 0;
 #pragma unroll
-            for (int rb = 0; rb < kColTileR / 16; ++rb) {
+            for (int rb = 0; rb < kNB; ++rb) {
                 const int64_t row = r0 + rb * 16;  // rows % 16 == 0: a block is whole or absent
                 if (row < a.rows) {
                     Raw<IT> raw;
-                    gather_col<IT>(s_tile, rb, tid, raw);
+                    gather_col<IT>(tb, rb, tid, raw);
                     uint64_t xp[8];
                     widen<IT>(raw, xp);
                     uint32_t code[2], scale;
                     encode_block<EM, Out::NONE>(xp, S, tbl, nz, code, scale, dummy);
-                    const int64_t b = col * nb_t + row / 16;
-                    st64(a.codes_t + b * 8, code[0], code[1]);
-                    st8(a.scales_t + b, scale);
+                    cw[2 * rb] = code[0];
+                    cw[2 * rb + 1] = code[1];
+                    sw |= scale << (8 * rb);
+                    if (!whole) {
+                        const int64_t blk = col * nb_t + row / 16;
+                        st64(a.codes_t + blk * 8, code[0], code[1]);
+                        st8(a.scales_t + blk, scale);
+                    }
+                }
+            }
+            if (whole) {
+                const int64_t blk = col * nb_t + r0 / 16;
+                if constexpr (kNB == 4) {
+                    st256(a.codes_t + blk * 8, cw);
+                    st32(a.scales_t + blk, sw);
+                } else {
+                    st128(a.codes_t + blk * 8, cw);
+                    st16(a.scales_t + blk, sw);
                 }
             }
         }
-        __syncthreads();  // the tile buffer is refilled next
+        __syncthreads();  // buffer b is refilled two tiles on
     }
 }
 

@@ -674,3 +674,20 @@ def test_quantize_colwise_full_size_sampled():
     oct_, ost, _ = oracle.quantize_colwise(xc, ocfg2, amax=a.cpu().numpy())
     assert np.array_equal(ct.cpu().numpy()[cols], oct_)
     assert np.array_equal(st.cpu().numpy()[cols], ost)
+
+
+def test_quantize_colwise_unaligned_outputs():
+    """Output buffers only 8-byte (codes) and 1-byte (scales) aligned take
+    the per-block stores instead of the wide ones; same bytes."""
+    gcfg, ocfg = _cfgs("mse", 448)
+    for dt in ("bf16", "f32"):
+        x = _x(128, 512, "F3", 140, dt)
+        R, C = x.shape
+        cb = torch.zeros(C * R // 2 + 64, dtype=torch.uint8, device=DEV)
+        sb = torch.zeros(C * R // 16 + 64, dtype=torch.uint8, device=DEV)
+        ct = cb[8:8 + C * R // 2].view(C, R // 2)
+        st = sb[1:1 + C * R // 16].view(C, R // 16)
+        _, _, a = fos.quantize_colwise(x.to(DEV), gcfg, codes_t=ct, scales_t=st)
+        torch.cuda.synchronize()
+        oc, os_, oa = oracle.quantize_colwise(x.float().numpy(), ocfg)
+        assert np.array_equal(ct.cpu().numpy(), oc) and np.array_equal(st.cpu().numpy(), os_)
