@@ -41,6 +41,20 @@ enum {
 
 FOS_API fos_status fos_diag_convert(int op, const void* in, void* out, int64_t n, fos_stream_t stream);
 
+/*
+ * fos_diag_wait_timeout -- runs one of the library's bounded waits against a
+ * condition that never comes true, so that its time limit and its error
+ * report can be checked without faulting or hanging the device:
+ *   which = 0: the wait of fos_qdq_fused's CTAs on a counter (word[1],
+ *              cleared by the call) that nothing increments; the wait gives
+ *              up and stores the workspace error code 1 in word[0];
+ *   which = 1: the column-wise kernel's wait on an mbarrier phase that no
+ *              copy completes; word[0] = 1 when the wait gave up.
+ * word: two uint32 of device memory owned by the caller.  One CTA runs for
+ * about a second; the device stays usable afterwards.
+ */
+FOS_API fos_status fos_diag_wait_timeout(int which, uint32_t* word, fos_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

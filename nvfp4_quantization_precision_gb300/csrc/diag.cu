@@ -68,4 +68,31 @@ cudaError_t launch_diag(int op, const void* in, void* out, int64_t n, cudaStream
     return cudaGetLastError();
 }
 
+// One of the library's bounded waits against a condition that never comes
+// true: which = 0, the fused launch's CTA-counter wait (counter word[1],
+// error word word[0]); which = 1, the column-wise kernel's mbarrier wait on
+// a phase nothing completes (word[0] = 1 when it gave up).
+__global__ void __launch_bounds__(kThreads) k_wait_timeout(int which, uint32_t* word) {
+    __shared__ float s_amax;
+    __shared__ __align__(8) uint64_t s_bar;
+    if (which == 0) {
+        fused_wait(&word[1], &word[1], 1u, &word[0], &s_amax);
+    } else {
+        if (threadIdx.x == 0) {
+            mbar_init(&s_bar, 1);
+            asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        }
+        __syncthreads();
+        const bool ok = mbar_wait(&s_bar, 0u);
+        if (threadIdx.x == 0) word[0] = ok ? 0u : 1u;
+    }
+}
+
+cudaError_t launch_wait_timeout(int which, uint32_t* word, cudaStream_t s) {
+    cudaError_t e = cudaMemsetAsync(word, 0, 2 * sizeof(uint32_t), s);
+    if (e != cudaSuccess) return e;
+    k_wait_timeout<<<1, kThreads, 0, s>>>(which, word);
+    return cudaGetLastError();
+}
+
 }  // namespace fos

@@ -645,6 +645,17 @@ fos_status fos_diag_convert(int op, const void* in, void* out, int64_t n, fos_st
     return cuda_status(launch_diag(op, in, out, n, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+fos_status fos_diag_wait_timeout(int which, uint32_t* word, fos_stream_t stream) {
+    if (which != 0 && which != 1) return FOS_ERR_INVALID_ARG;
+    if (!word) return FOS_ERR_INVALID_ARG;
+    if (!aligned(word, 4)) return FOS_ERR_MISALIGNED;
+    const int dev = device_of(word);
+    if (dev < 0) return FOS_ERR_INVALID_ARG;
+    DeviceScope scope(dev);
+    if (scope.st) return scope.st;
+    return cuda_status(launch_wait_timeout(which, word, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 }  // extern "C"
 
 // ------------------------------------------------------------ fused amax + QDQ

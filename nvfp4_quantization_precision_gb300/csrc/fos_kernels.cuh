@@ -393,7 +393,7 @@ struct ColTile {
     static constexpr int kElt = (IT == In::F32) ? 4 : 2;
     static constexpr int kBytes = kR * kC * kElt;          // 32 KiB
 };
-constexpr uint32_t kMbarSpins = 1u << 22;
+constexpr uint32_t kMbarSpins = 1u << 20;  // tries of at most about 1 us each
 
 struct ColArgs {
     CUtensorMap tmap;   // x as [rows, cols], box kR x 256 (2D TMA)
@@ -423,7 +423,8 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
     for (uint32_t i = 0; i < kMbarSpins; ++i) {
         uint32_t done;
-        asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        asm volatile("{\n\t.reg .pred p;\n\t"
+                     "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, 1000;\n\t"
                      "selp.u32 %0, 1, 0, p;\n\t}"
                      : "=r"(done) : "r"(smem_u32(bar)), "r"(parity) : "memory");
         if (done) return true;
@@ -942,11 +943,79 @@ __global__ void __launch_bounds__(kThreads) k_dequant(const DeqArgs a) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     float2* tbl = s_tbl[warp];
     const int64_t nw = (int64_t)gridDim.x * kWarps, gw = (int64_t)blockIdx.x * kWarps + warp;
+    const int64_t cols = a.nb * 16;
+    char* ob = static_cast<char*>(a.out);
+    if constexpr (SRC == Src::TENSOR) {
+        // one scale for the tensor: the blocks are walked grid-stride as one
+        // flat sequence (codes and outputs are block-major; a 1x16 scale is
+        // per block, a 16x16 scale per (row / 16, block)), with the next
+        // block's code word and scale byte loaded a step ahead
+        build_table(tbl, global_scale(a.amax[0], a.six_bound), lane);
+        const int64_t nblk = a.rows * a.nb, step = nw * 32;
+        int64_t b = gw * 32 + lane;
+        // 16x16: (row, column block) of b, advanced by step each iteration
+        int64_t brow = B16 ? b / a.nb : 0, bcol = B16 ? b % a.nb : 0;
+        const int64_t srow = B16 ? step / a.nb : 0, scol = B16 ? step % a.nb : 0;
+        auto scale_at = [&](int64_t blk, int64_t r, int64_t j) -> uint32_t {
+            return B16 ? a.scales[(r >> 4) * a.nb + j] : a.scales[blk];
+        };
+        uint2 cw = make_uint2(0u, 0u);
+        uint32_t sb = 0;
+        if (b < nblk) {
+            cw = *reinterpret_cast<const uint2*>(a.codes + b * 8);
+            sb = scale_at(b, brow, bcol);
+        }
+        for (; b - lane < nblk; b += step) {
+            const int64_t bn = b + step;
+            if constexpr (B16) {
+                brow += srow;
+                bcol += scol;
+                if (bcol >= a.nb) {
+                    bcol -= a.nb;
+                    ++brow;
+                }
+            }
+            uint2 cwn = make_uint2(0u, 0u);
+            uint32_t sbn = 0;
+            if (bn < nblk) {
+                cwn = *reinterpret_cast<const uint2*>(a.codes + bn * 8);
+                sbn = scale_at(bn, brow, bcol);
+            }
+            if (b < nblk) {
+                const float d = tbl[sb & 0x7Fu].y;
+                // sigma / S is odd in sigma; a zero scale of either sign decodes by +0
+                const float dsig = ((sb & 0x80u) && d != 0.0f) ? -d : d;
+                const uint64_t dd = pk(dsig, dsig);
+                uint32_t outw[16];
+#pragma unroll
+                for (int p = 0; p < 8; ++p) {
+                    const uint32_t byte = ((p < 4 ? cw.x : cw.y) >> (8 * (p & 3))) & 0xFFu;
+                    const uint64_t v = mul2(f16x2_f32x2(e2m1x2_f16x2(byte)), dd);
+                    if constexpr (OT == Out::F32) {
+                        float lo, hi;
+                        upk(v, lo, hi);
+                        outw[2 * p] = __float_as_uint(lo);
+                        outw[2 * p + 1] = __float_as_uint(hi);
+                    } else {
+                        outw[p] = out_pair<OT>(v);
+                    }
+                }
+                if constexpr (OT == Out::F32) {
+                    st256(ob + b * 64, outw);
+                    st256(ob + b * 64 + 32, outw + 8);
+                } else {
+                    st256(ob + b * 32, outw);
+                }
+            }
+            cw = cwn;
+            sb = sbn;
+        }
+        return;
+    }
     const int64_t u0 = split_at(a.units, nw, gw), u1 = split_at(a.units, nw, gw + 1);
     if (u0 >= u1) return;
     int64_t row = u0 / a.cpr, chunk = u0 % a.cpr;
     int64_t key = -1;
-    const int64_t cols = a.nb * 16;
     for (int64_t u = u0; u < u1; ++u) {
         const int64_t k = (SRC == Src::ROW) ? (B16 ? row - (row & 15) : row) : 0;
         if (k != key) {
@@ -976,7 +1045,6 @@ __global__ void __launch_bounds__(kThreads) k_dequant(const DeqArgs a) {
                     outw[p] = out_pair<OT>(v);
                 }
             }
-            char* ob = static_cast<char*>(a.out);
             if constexpr (OT == Out::F32) {
                 st256(ob + (row * cols + j * 16) * 4, outw);
                 st256(ob + (row * cols + j * 16) * 4 + 32, outw + 8);

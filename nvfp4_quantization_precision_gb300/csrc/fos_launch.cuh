@@ -123,5 +123,6 @@ cudaError_t launch_pipe(In, Err, const PipeArgs&, cudaStream_t);
 cudaError_t launch_dequant(Out, bool b16, Src, const DeqArgs&, cudaStream_t);
 cudaError_t launch_amax(In, Src, const AmaxArgs&, cudaStream_t);
 cudaError_t launch_diag(int op, const void* in, void* out, int64_t n, cudaStream_t);
+cudaError_t launch_wait_timeout(int which, uint32_t* word, cudaStream_t);
 
 }  // namespace fos

@@ -222,3 +222,10 @@ def test_quantize_colwise_rejects_before_any_cuda_call(L):
     assert call(cfg=_cfg(block=1)) == fos.FOS_ERR_UNSUPPORTED
     assert call(cfg=_cfg(granularity=1)) == fos.FOS_ERR_UNSUPPORTED
     assert call(codes=None) == fos.FOS_ERR_INVALID_ARG        # codes and scales go together
+
+
+def test_diag_wait_timeout_rejects_bad_arguments(L):
+    L.fos_diag_wait_timeout.restype = ctypes.c_int
+    assert L.fos_diag_wait_timeout(2, FAKE, None) == fos.FOS_ERR_INVALID_ARG
+    assert L.fos_diag_wait_timeout(0, None, None) == fos.FOS_ERR_INVALID_ARG
+    assert L.fos_diag_wait_timeout(0, ctypes.c_void_p(0x10002), None) == fos.FOS_ERR_MISALIGNED

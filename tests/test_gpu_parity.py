@@ -2,6 +2,7 @@
 identical seeded bytes.  Tolerance 0 everywhere: codes, scales, amax and
 outputs are compared as integer views, so signed zeros and NaN payloads of
 the outputs count."""
+import ctypes
 import itertools
 
 import numpy as np
@@ -691,3 +692,21 @@ def test_quantize_colwise_unaligned_outputs():
         torch.cuda.synchronize()
         oc, os_, oa = oracle.quantize_colwise(x.float().numpy(), ocfg)
         assert np.array_equal(ct.cpu().numpy(), oc) and np.array_equal(st.cpu().numpy(), os_)
+
+
+# ------------------------------------------------------------------ bounded waits
+@pytest.mark.parametrize("which", [0, 1])
+def test_bounded_waits_give_up_and_report(which):
+    """A wait whose condition never comes true (a counter nothing increments,
+    an mbarrier phase no copy completes) gives up after about a second and
+    reports it; the device keeps working afterwards."""
+    L = fos.lib()
+    L.fos_diag_wait_timeout.argtypes = [ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]
+    L.fos_diag_wait_timeout.restype = ctypes.c_int
+    word = torch.full((2,), 7, dtype=torch.int32, device=DEV)
+    s = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    assert L.fos_diag_wait_timeout(which, word.data_ptr(), s) == fos.FOS_OK
+    torch.cuda.synchronize()
+    assert int(word[0]) == 1
+    x = _x(64, 256, "F1", 150, "bf16")
+    _check_quant(x, *_cfgs("mse"), amax_given=False)
