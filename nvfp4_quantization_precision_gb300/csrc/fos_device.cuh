@@ -76,7 +76,6 @@ __device__ __forceinline__ uint64_t sub2(uint64_t a, uint64_t b) {
     asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
     return r;
 }
-__device__ __forceinline__ uint64_t abs2(uint64_t a) { return a & 0x7FFFFFFF7FFFFFFFull; }
 // rn(a * b) per lane, written as fma(a, b, c) with c = (-0, -0) supplied at run
 // time.  Adding -0 is exact and keeps the sign of a zero product, so the
 // result is the correctly rounded product; because it is already a fused
@@ -97,15 +96,6 @@ __device__ __forceinline__ uint32_t e2m1x2(uint64_t y) {
         "cvt.rn.satfinite.e2m1x2.f32 q, hi, lo;\n\tcvt.u32.u8 %0, q;\n\t}"
         : "=r"(r) : "l"(y));
     return r;
-}
-// Encode a pair to E2M1 and decode the result in one step: `byte` receives
-// the packed codes (low nibble = low element), `h` their exact values as
-// f16x2 (low half = low element).
-__device__ __forceinline__ void e2m1x2_enc_dec(uint64_t y, uint32_t& byte, uint32_t& h) {
-    asm("{\n\t.reg .b8 q;\n\t.reg .f32 lo, hi;\n\tmov.b64 {lo, hi}, %2;\n\t"
-        "cvt.rn.satfinite.e2m1x2.f32 q, hi, lo;\n\tcvt.rn.f16x2.e2m1x2 %1, q;\n\t"
-        "cvt.u32.u8 %0, q;\n\t}"
-        : "=r"(byte), "=r"(h) : "l"(y));
 }
 // Four pairs at once: encode y[0..3] to E2M1, return the four code bytes
 // packed into one word (byte k = pair k, low nibble = low element) and, with
@@ -219,12 +209,6 @@ __device__ __forceinline__ void ld256h(const void* p, uint32_t* w) {
             : "l"(p), "l"(l2_policy<H>()));
     }
 }
-// Hint the memory system to bring [p, p + bytes) into L2 (bytes a multiple of
-// 16, p 16-byte aligned).  Nothing waits for it; a later load just finds the
-// data closer.
-__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
-}
 __device__ __forceinline__ void st256(void* p, const uint32_t* w) {
     asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(w[0]),
                  "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
@@ -336,9 +320,6 @@ __device__ __forceinline__ void fill_table_cta(float2* tbl, float S, int tid) {
     reinterpret_cast<float*>(tbl)[2 * c + (tid >> 7)] = v;
 }
 
-__device__ __forceinline__ uint32_t pack4(uint32_t b0, uint32_t b1, uint32_t b2, uint32_t b3) {
-    return __byte_perm(__byte_perm(b0, b1, 0x0040), __byte_perm(b2, b3, 0x0040), 0x5410);
-}
 
 // Output element types of the decode paths.
 enum class Out : int { NONE = 0, BF16 = 1, F16 = 2, F32 = 3 };
