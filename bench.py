@@ -534,6 +534,13 @@ def _rows(fos, xs, stream, peak, only=None):
             ms = _graph_ms(lambda: fos.qdq(ws_, c, amaxes=wam, outs=wout), 2, stream)
             rec("qdq_list_8x4096x6144_bf16_" + mode, sum(t.numel() for t in ws_) * 4, ms)
         del ws_, wout
+    if want("swizzle"):
+        # 1x16 block scales of the activation into the tiled GEMM layout
+        sw = torch.empty(ROWS * COLS // 16, dtype=torch.uint8, device=dev)
+        fos.quantize(xs[0], fos.Config(), amax=am[0], codes=codes, scales=scales)
+        ms = _graph_ms(lambda: fos.swizzle_scales(scales, ROWS, COLS, out=sw), R8, stream)
+        rec("swizzle_scales_8192x4096", 2 * ROWS * COLS // 16, ms)
+        del sw
     if want("dequant"):
         # a11: dequantize back to bf16
         c = fos.Config()
@@ -646,7 +653,7 @@ def main():
                     help="only the timed step (no e2e / per-row / CPU baseline)")
     ap.add_argument("--rows-only", default="",
                     help="comma list of row sections to time alone (amax, encode, colwise, qdq, "
-                         "qdq_list, qdq_page, dequant, grouped, weight, experts); no step")
+                         "qdq_list, qdq_page, swizzle, dequant, grouped, weight, experts); no step")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -175,6 +175,21 @@ FOS_API fos_status fos_quantize_colwise(const void* x, fos_dtype dt, int64_t row
                                         fos_stream_t stream);
 
 /*
+ * fos_swizzle_scales -- the 1x16 block scales of a [rows, cols] tensor
+ * (scales [rows, cols/16], as fos_quantize writes them) rearranged into the
+ * tiled layout that block-scaled FP4 GEMMs read: the scale matrix is padded
+ * with zero bytes to a multiple of 128 rows and 4 columns and cut into
+ * 128 x 4 tiles of 512 bytes, stored tile-row by tile-row; inside a tile,
+ * scale (32 i + j, k) (i < 4, j < 32, k < 4) is byte 16 j + 4 i + k.
+ * out holds fos_swizzled_scales_bytes(rows, cols) bytes (4-byte aligned).
+ * The pages pass plain scales to their GEMMs; this is the layout a GEMM
+ * library's NVFP4 path takes, checked in the tests against such a GEMM.
+ */
+FOS_API int64_t fos_swizzled_scales_bytes(int64_t rows, int64_t cols);
+FOS_API fos_status fos_swizzle_scales(const uint8_t* scales, int64_t rows, int64_t cols,
+                                      uint8_t* out, fos_stream_t stream);
+
+/*
  * fos_dequantize -- standard NVFP4 decode (grouped PR, first commit:
  * "nvfp4_dequantize: the standard NVFP4 decode (recipe-agnostic)"):
  *   out = round_to(out_dt, e2m1(code) * (e4m3(scale) / S)),

@@ -290,6 +290,28 @@ def quantize_colwise(x, cfg=Config(), amax=None, codes_t=None, scales_t=None, ro
     return codes_t, scales_t, amax
 
 
+def swizzle_scales(scales, rows, cols, out=None):
+    """fos_swizzle_scales: 1x16 scales [rows, cols/16] in the tiled layout of
+    block-scaled FP4 GEMMs (a flat uint8 tensor, zero padded)."""
+    _cuda(scales, "scales")
+    L = lib()
+    if not getattr(L, "_swizzle_declared", False):
+        L.fos_swizzled_scales_bytes.argtypes = [ctypes.c_int64, ctypes.c_int64]
+        L.fos_swizzled_scales_bytes.restype = ctypes.c_int64
+        L.fos_swizzle_scales.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64,
+                                         ctypes.c_void_p, ctypes.c_void_p]
+        L.fos_swizzle_scales.restype = ctypes.c_int
+        L._swizzle_declared = True
+    nbytes = L.fos_swizzled_scales_bytes(rows, cols)
+    if nbytes < 0:
+        raise ValueError("bad shape for swizzled scales")
+    if out is None:
+        out = torch.empty(nbytes, dtype=torch.uint8, device=scales.device)
+    _check(L.fos_swizzle_scales(_p(scales), rows, cols, _p(out), _stream(scales)),
+           "fos_swizzle_scales")
+    return out
+
+
 def qdq_fused_workspace(n, device):
     """A workspace for fos_qdq_fused over n tensors (caller-side allocation)."""
     nb = lib().fos_qdq_fused_workspace_bytes(int(n))

@@ -809,3 +809,28 @@ fos_status fos_quantize_colwise(const void* x, fos_dtype dt, int64_t rows, int64
 
 }  // extern "C"
 
+// ------------------------------------------------------------ swizzled scales
+extern "C" {
+
+int64_t fos_swizzled_scales_bytes(int64_t rows, int64_t cols) {
+    if (rows < 0 || cols < 0 || cols % 16 != 0) return -1;
+    return (rows + 127) / 128 * 128 * ((cols / 16 + 3) / 4 * 4);
+}
+
+fos_status fos_swizzle_scales(const uint8_t* scales, int64_t rows, int64_t cols, uint8_t* out,
+                              fos_stream_t stream) {
+    fos_status st = check_shape(rows, cols, false);
+    if (st) return st;
+    if (rows == 0 || cols == 0) return FOS_OK;
+    if (!scales || !out) return FOS_ERR_INVALID_ARG;
+    if (!aligned(out, 4)) return FOS_ERR_MISALIGNED;
+    const int dev = common_device({scales, out});
+    if (dev < 0) return FOS_ERR_INVALID_ARG;
+    DeviceScope scope(dev);
+    if (scope.st) return scope.st;
+    return cuda_status(launch_swizzle(scales, rows, cols / 16, out,
+                                      reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"
+

@@ -124,5 +124,7 @@ cudaError_t launch_dequant(Out, bool b16, Src, const DeqArgs&, cudaStream_t);
 cudaError_t launch_amax(In, Src, const AmaxArgs&, cudaStream_t);
 cudaError_t launch_diag(int op, const void* in, void* out, int64_t n, cudaStream_t);
 cudaError_t launch_wait_timeout(int which, uint32_t* word, cudaStream_t);
+cudaError_t launch_swizzle(const uint8_t* scales, int64_t rows, int64_t nb, uint8_t* out,
+                           cudaStream_t);
 
 }  // namespace fos

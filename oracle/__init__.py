@@ -228,6 +228,24 @@ def quantize_colwise(x, cfg: Config, amax=None):
     return quantize(np.ascontiguousarray(_f32(x).T), cfg, amax=amax)
 
 
+def swizzle_scales(scales):
+    """Scales [R, C/16] in the tiled layout of block-scaled FP4 GEMMs: padded
+    with zeros to a multiple of 128 rows and 4 columns, cut into 128 x 4
+    tiles of 512 bytes stored tile-row by tile-row; inside a tile, scale
+    (32 i + j, k) is byte 16 j + 4 i + k."""
+    s = np.ascontiguousarray(scales, dtype=np.uint8)
+    R, NB = s.shape
+    PR, PC = -(-R // 128) * 128, -(-NB // 4) * 4
+    pad = np.zeros((PR, PC), np.uint8)
+    pad[:R, :NB] = s
+    r = np.arange(PR)[:, None]
+    c = np.arange(PC)[None, :]
+    off = ((r // 128) * (PC // 4) + c // 4) * 512 + (r % 32) * 16 + ((r % 128) // 32) * 4 + c % 4
+    out = np.zeros(PR * PC, np.uint8)
+    out[off.ravel()] = pad.ravel()
+    return out
+
+
 _OUTK = {"f32": (OUT_F32, np.float32), "bf16": (OUT_BF16, np.uint16), "f16": (OUT_F16, np.uint16)}
 
 

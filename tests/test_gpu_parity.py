@@ -710,3 +710,42 @@ def test_bounded_waits_give_up_and_report(which):
     assert int(word[0]) == 1
     x = _x(64, 256, "F1", 150, "bf16")
     _check_quant(x, *_cfgs("mse"), amax_given=False)
+
+
+# ------------------------------------------------------------------ tiled scale layout
+@pytest.mark.parametrize("shape", [(1, 16), (128, 64), (200, 144), (8192, 4096)])
+def test_swizzle_scales(shape):
+    R, C = shape
+    s = np.random.default_rng(R + C).integers(0, 0x7F, (R, C // 16), dtype=np.uint8)
+    got = fos.swizzle_scales(torch.from_numpy(s).to(DEV), R, C)
+    torch.cuda.synchronize()
+    assert np.array_equal(got.cpu().numpy(), oracle.swizzle_scales(s))
+
+
+@pytest.mark.parametrize("mode", ["std", "mse"])
+def test_swizzled_scales_feed_an_fp4_gemm(mode):
+    """Codes and tiled scales from this library, handed to PyTorch's NVFP4
+    scaled matmul, give the product of the dequantized operands: the tiled
+    layout is the one such a GEMM reads."""
+    if not hasattr(torch, "float4_e2m1fn_x2"):
+        pytest.skip("no FP4 dtype in this PyTorch")
+    M, N, K = 256, 128, 512
+    gcfg, _ = _cfgs(mode)
+    a = workloads.activation(M, K, "F1", seed=31, device=DEV)
+    b = workloads.activation(N, K, "F3", seed=32, device=DEV)
+    ca, sa, aa = fos.quantize(a, gcfg)
+    cb, sb, ab = fos.quantize(b, gcfg)
+    swa, swb = fos.swizzle_scales(sa, M, K), fos.swizzle_scales(sb, N, K)
+    try:
+        got = torch._scaled_mm(ca.view(torch.float4_e2m1fn_x2), cb.view(torch.float4_e2m1fn_x2).t(),
+                               swa.view(torch.float8_e4m3fn), swb.view(torch.float8_e4m3fn),
+                               out_dtype=torch.float32)
+    except (RuntimeError, TypeError) as e:
+        pytest.skip("no NVFP4 scaled matmul here: %s" % str(e)[:80])
+    da = fos.dequantize(ca, sa, aa, gcfg, out_dtype=torch.float32).double()
+    db = fos.dequantize(cb, sb, ab, gcfg, out_dtype=torch.float32).double()
+    Sa = float(oracle.global_scale(float(aa[0]), 448))
+    Sb = float(oracle.global_scale(float(ab[0]), 448))
+    ref = (da * Sa) @ (db * Sb).t()
+    err = (got.double() - ref).abs().max().item()
+    assert err <= 1e-5 * ref.abs().max().item() + 1e-6, err

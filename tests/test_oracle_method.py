@@ -542,3 +542,25 @@ def test_colwise_of_a_symmetric_matrix_is_the_rowwise_result(orc):
     cfg = orc.Config(four_over_six=True, mse=False, err_f16=True)
     assert all(np.array_equal(p, q) for p, q in zip(orc.quantize_colwise(x, cfg),
                                                       orc.quantize(x, cfg)))
+
+
+# ---------------------------------------------------------------- tiled scale layout
+def test_swizzled_scale_layout_offsets(orc):
+    """Hand-placed bytes of a 200 x 9 scale matrix (2 tile rows, 3 tile
+    columns after padding to 256 x 12) land where the layout puts them, the
+    layout is a permutation, and the padding is zero."""
+    s = np.zeros((200, 9), np.uint8)
+    marks = {(0, 0): 0, (1, 0): 16, (31, 0): 496, (32, 0): 4, (96, 0): 12, (127, 3): 511,
+             (0, 1): 1, (0, 4): 512, (5, 6): 512 + 5 * 16 + 2, (128, 0): 3 * 512,
+             (199, 8): (3 + 2) * 512 + (71 % 32) * 16 + (71 // 32) * 4 + 0}
+    for i, (rc, _) in enumerate(marks.items()):
+        s[rc] = i + 1
+    out = orc.swizzle_scales(s)
+    assert out.size == 256 * 12
+    for i, (rc, off) in enumerate(marks.items()):
+        assert out[off] == i + 1, (rc, off)
+    assert np.count_nonzero(out) == len(marks)
+    full = np.arange(256 * 12, dtype=np.int64).reshape(256, 12)
+    # a bijection on the padded matrix: every byte of a distinct-valued input appears once
+    vals = (full % 251 + 1).astype(np.uint8)
+    assert np.array_equal(np.sort(orc.swizzle_scales(vals)), np.sort(vals.ravel()))
