@@ -54,6 +54,14 @@ def _peaks():
         return 6800.0, "fallback"
 
 
+def _bf16_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"])
+    except Exception:
+        return 1900.0
+
+
 def kernel_source_hash():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "nvfp4_quantization_precision_gb300", "csrc")
@@ -541,6 +549,24 @@ def _rows(fos, xs, stream, peak, only=None):
         ms = _graph_ms(lambda: fos.swizzle_scales(scales, ROWS, COLS, out=sw), R8, stream)
         rec("swizzle_scales_8192x4096", 2 * ROWS * COLS // 16, ms)
         del sw
+    if want("mm"):
+        # the forward product of quantized operands: activation 8192x4096
+        # (per-tensor scale) times a 14336x4096 weight, fp32 out; TFLOP/s against
+        # the FP4 peak taken as the measured bf16 peak x 6 (nominal 13.5 / 2.25)
+        M, N, K = ROWS, 14336, COLS
+        c = fos.Config()
+        w = workloads.weight(N, K, seed=0, device=dev)
+        ca, sa, aa = fos.quantize(xs[0], c)
+        cw, sw, aw = fos.quantize(w, c)
+        ta, tw = fos.swizzle_scales(sa, M, K), fos.swizzle_scales(sw, N, K)
+        mo = torch.empty(M, N, dtype=torch.float32, device=dev)
+        ms = _graph_ms(lambda: fos.mm(ca, ta, aa, cw, tw, aw, c, out=mo), 4, stream)
+        tf = 2.0 * M * N * K / (ms / 1e3) / 1e12
+        fp4_peak = _bf16_peak() * 6
+        res["mm_fp4_8192x14336x4096"] = {"TFLOP/s": round(tf, 1), "us": round(ms * 1e3, 2),
+                                         "frac": round(tf / fp4_peak, 3),
+                                         "peak": "measured bf16 x 6 = %.0f TFLOP/s" % fp4_peak}
+        del w, mo
     if want("dequant"):
         # a11: dequantize back to bf16
         c = fos.Config()
@@ -653,7 +679,7 @@ def main():
                     help="only the timed step (no e2e / per-row / CPU baseline)")
     ap.add_argument("--rows-only", default="",
                     help="comma list of row sections to time alone (amax, encode, colwise, qdq, "
-                         "qdq_list, qdq_page, swizzle, dequant, grouped, weight, experts); no step")
+                         "qdq_list, qdq_page, swizzle, mm, dequant, grouped, weight, experts); no step")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -190,6 +190,27 @@ FOS_API fos_status fos_swizzle_scales(const uint8_t* scales, int64_t rows, int64
                                       uint8_t* out, fos_stream_t stream);
 
 /*
+ * fos_mm -- out = a . b^T from quantized operands, the forward product of
+ * the grouped PR's four_over_six_mm: a [M, K] and b [N, K] were quantized
+ * with 1x16 blocks (codes [M, K/2] and [N, K/2]) and their block scales put
+ * into the tiled GEMM layout (fos_swizzle_scales); a_amax / b_amax are the
+ * amaxes they were quantized with (a: [M] when cfg->granularity is
+ * FOS_SCALE_ROW, else [1]; b: [1]).  The block-scaled product D runs as a
+ * cuBLASLt NVFP4 GEMM (a library GEMM: fp32 accumulation, no workspace);
+ * this library's epilogue then applies the global decode scales,
+ *   out[m][n] = (D[m][n] * g_a(m)) * g_b,  g = rn(1 / S),
+ * S the global scale fos_quantize used (cfg->e4m3_bound).  out: fp32 [M, N]
+ * row-major, 16-byte aligned, like all operands.  M and N multiples of 16,
+ * K a multiple of 64; FOS_ERR_UNSUPPORTED when cuBLASLt offers no
+ * algorithm.  The first call on a device creates its cuBLASLt handle.
+ */
+FOS_API fos_status fos_mm(const uint8_t* a_codes, const uint8_t* a_scales_tiled,
+                          const float* a_amax, const uint8_t* b_codes,
+                          const uint8_t* b_scales_tiled, const float* b_amax, int64_t M,
+                          int64_t N, int64_t K, const fos_config* cfg, float* out,
+                          fos_stream_t stream);
+
+/*
  * fos_dequantize -- standard NVFP4 decode (grouped PR, first commit:
  * "nvfp4_dequantize: the standard NVFP4 decode (recipe-agnostic)"):
  *   out = round_to(out_dt, e2m1(code) * (e4m3(scale) / S)),

@@ -312,6 +312,30 @@ def swizzle_scales(scales, rows, cols, out=None):
     return out
 
 
+def mm(a_codes, a_scales_tiled, a_amax, b_codes, b_scales_tiled, b_amax, cfg=Config(),
+       out=None):
+    """fos_mm: a . b^T (fp32 [M, N]) from a's and b's 1x16 codes, tiled scales
+    (swizzle_scales) and amaxes; cfg.row_scaled when a was quantized with a
+    per-row scale."""
+    _cuda(a_codes, "a_codes")
+    M, K2 = a_codes.shape
+    N = b_codes.shape[0]
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float32, device=a_codes.device)
+    L = lib()
+    if not getattr(L, "_mm_declared", False):
+        P = ctypes.c_void_p
+        L.fos_mm.argtypes = [P, P, P, P, P, P, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                             ctypes.POINTER(FosConfig), P, P]
+        L.fos_mm.restype = ctypes.c_int
+        L._mm_declared = True
+    cc = cfg.c(True)
+    _check(L.fos_mm(_p(a_codes), _p(a_scales_tiled), _p(a_amax), _p(b_codes), _p(b_scales_tiled),
+                    _p(b_amax), M, N, 2 * K2, ctypes.byref(cc), _p(out), _stream(a_codes)),
+           "fos_mm")
+    return out
+
+
 def qdq_fused_workspace(n, device):
     """A workspace for fos_qdq_fused over n tensors (caller-side allocation)."""
     nb = lib().fos_qdq_fused_workspace_bytes(int(n))

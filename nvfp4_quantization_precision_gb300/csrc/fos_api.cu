@@ -834,3 +834,41 @@ fos_status fos_swizzle_scales(const uint8_t* scales, int64_t rows, int64_t cols,
 
 }  // extern "C"
 
+// ------------------------------------------------------------ product of quantized operands
+extern "C" {
+
+fos_status fos_mm(const uint8_t* a_codes, const uint8_t* a_scales_tiled, const float* a_amax,
+                  const uint8_t* b_codes, const uint8_t* b_scales_tiled, const float* b_amax,
+                  int64_t M, int64_t N, int64_t K, const fos_config* cfg, float* out,
+                  fos_stream_t stream) {
+    fos_status st = check_config(cfg);
+    if (st) return st;
+    if (cfg->block != FOS_BLOCK_1X16) return FOS_ERR_UNSUPPORTED;
+    if (M < 0 || N < 0 || K < 0) return FOS_ERR_INVALID_ARG;
+    if (M % 16 || N % 16 || K % 64) return FOS_ERR_UNSUPPORTED;
+    if (M >= (INT64_C(1) << 31) || N >= (INT64_C(1) << 31) || K >= (INT64_C(1) << 31))
+        return FOS_ERR_UNSUPPORTED;
+    if (M == 0 || N == 0) return FOS_OK;
+    if (!a_codes || !a_scales_tiled || !a_amax || !b_codes || !b_scales_tiled || !b_amax || !out)
+        return FOS_ERR_INVALID_ARG;
+    if (!aligned(a_codes, 16) || !aligned(b_codes, 16) || !aligned(a_scales_tiled, 16) ||
+        !aligned(b_scales_tiled, 16) || !aligned(out, 16))
+        return FOS_ERR_MISALIGNED;
+    const int dev = common_device({a_codes, a_scales_tiled, a_amax, b_codes, b_scales_tiled,
+                                   b_amax, out});
+    if (dev < 0) return FOS_ERR_INVALID_ARG;
+    DeviceScope scope(dev);
+    if (scope.st) return scope.st;
+    if (K == 0) {  // empty sum
+        return cuda_status(cudaMemsetAsync(out, 0, sizeof(float) * (size_t)(M * N),
+                                           reinterpret_cast<cudaStream_t>(stream)));
+    }
+    const int rc = run_mm(a_codes, a_scales_tiled, a_amax, cfg->granularity == FOS_SCALE_ROW,
+                          b_codes, b_scales_tiled, b_amax, M, N, K,
+                          6.0f * (float)cfg->e4m3_bound, out, dev,
+                          reinterpret_cast<cudaStream_t>(stream));
+    return rc == 0 ? FOS_OK : (rc == 1 ? FOS_ERR_UNSUPPORTED : FOS_ERR_CUDA);
+}
+
+}  // extern "C"
+

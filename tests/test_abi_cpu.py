@@ -229,3 +229,20 @@ def test_diag_wait_timeout_rejects_bad_arguments(L):
     assert L.fos_diag_wait_timeout(2, FAKE, None) == fos.FOS_ERR_INVALID_ARG
     assert L.fos_diag_wait_timeout(0, None, None) == fos.FOS_ERR_INVALID_ARG
     assert L.fos_diag_wait_timeout(0, ctypes.c_void_p(0x10002), None) == fos.FOS_ERR_MISALIGNED
+
+
+def test_mm_rejects_before_any_cuda_call(L):
+    L.fos_mm.restype = ctypes.c_int
+    c = _cfg()
+    i64 = ctypes.c_int64
+
+    def call(M=16, N=16, K=64, cfg=c, a=FAKE):
+        return L.fos_mm(a, FAKE, FAKE, FAKE, FAKE, FAKE, i64(M), i64(N), i64(K), ctypes.byref(cfg),
+                        FAKE, None)
+    assert call(K=48) == fos.FOS_ERR_UNSUPPORTED
+    assert call(M=8) == fos.FOS_ERR_UNSUPPORTED
+    assert call(cfg=_cfg(block=1)) == fos.FOS_ERR_UNSUPPORTED
+    assert call(M=-16) == fos.FOS_ERR_INVALID_ARG
+    assert call(a=None) == fos.FOS_ERR_INVALID_ARG
+    assert call(a=ctypes.c_void_p(0x10008)) == fos.FOS_ERR_MISALIGNED
+    assert call(M=0) == fos.FOS_OK

@@ -749,3 +749,46 @@ def test_swizzled_scales_feed_an_fp4_gemm(mode):
     ref = (da * Sa) @ (db * Sb).t()
     err = (got.double() - ref).abs().max().item()
     assert err <= 1e-5 * ref.abs().max().item() + 1e-6, err
+
+
+# ------------------------------------------------------------------ product of quantized operands
+def _block_values(codes, scales):
+    """v * sigma per element (exact in binary64) from 1x16 codes and scales."""
+    R, C2 = codes.shape
+    lo = (codes & 0xF).astype(np.uint32)
+    hi = (codes >> 4).astype(np.uint32)
+    q = np.empty((R, 2 * C2), np.uint32)
+    q[:, 0::2], q[:, 1::2] = lo, hi
+    v = np.vectorize(oracle.e2m1_value, otypes=[np.float64])(q)
+    sig = np.vectorize(oracle.e4m3_value, otypes=[np.float64])(scales.astype(np.uint32))
+    return v * np.repeat(sig, 16, axis=1)
+
+
+@pytest.mark.parametrize("mode", ["std", "mse"])
+@pytest.mark.parametrize("row", [False, True])
+def test_mm_of_quantized_operands(mode, row):
+    """a . b^T from this library's codes and tiled scales equals the product
+    of the oracle's block values of the same inputs, divided by the global
+    scales, within the fp32 accumulation bound (K + 2) * 2^-24 * sum |terms|."""
+    M, N, K = 256, 128, 512
+    gcfg_a, ocfg_a = _cfgs(mode, 448, row)
+    gcfg_b, ocfg_b = _cfgs(mode, 448)
+    a = _x(M, K, "F2", 51, "bf16")
+    b = _x(N, K, "F1", 52, "bf16")
+    ca, sa, aa = fos.quantize(a.to(DEV), gcfg_a)
+    cb, sb, ab = fos.quantize(b.to(DEV), gcfg_b)
+    out = fos.mm(ca, fos.swizzle_scales(sa, M, K), aa, cb, fos.swizzle_scales(sb, N, K), ab,
+                 gcfg_a)
+    torch.cuda.synchronize()
+    oca, osa, oaa = oracle.quantize(a.float().numpy(), ocfg_a)
+    ocb, osb, oab = oracle.quantize(b.float().numpy(), ocfg_b)
+    assert np.array_equal(ca.cpu().numpy(), oca) and np.array_equal(cb.cpu().numpy(), ocb)
+    pa, pb = _block_values(oca, osa), _block_values(ocb, osb)
+    D = pa @ pb.T
+    bound = (K + 2) * 2.0 ** -24 * (np.abs(pa) @ np.abs(pb).T)
+    ga = 1.0 / np.array([oracle.global_scale(float(v), 448) for v in oaa], np.float32)
+    gb = 1.0 / np.float32(oracle.global_scale(float(oab[0]), 448))
+    ga = ga.reshape(-1, 1) if row else ga.reshape(1, 1)
+    ref = D * ga * gb
+    err = np.abs(out.cpu().numpy().astype(np.float64) - ref)
+    assert np.all(err <= bound * np.abs(ga * gb) + 1e-30), float((err / (bound * np.abs(ga * gb) + 1e-30)).max())
