@@ -63,13 +63,14 @@ def _bf16_peak():
 
 
 def kernel_source_hash():
+    """Hash of the sources the profiled pipeline kernel is built from (its
+    device code and its launcher); other library files do not change it."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "nvfp4_quantization_precision_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode())
-                h.update(f.read())
+    for name in ("fos_device.cuh", "fos_kernels.cuh", "pipe.cu"):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
     return h.hexdigest()[:16]
 
 
