@@ -13,24 +13,29 @@
  * pinned width-16 error reduction, NaN-dropping block amax, NaN -> +6).
  *
  * Conventions shared by every entry point
- *   - Data pointers (x, out, codes, scales, amax, offs) are DEVICE pointers
- *     owned by the caller; the library never allocates, frees or keeps them.
- *     Host-side arrays (the pointer / size lists of fos_qdq) are read during
- *     the call only.
+ *   - Data pointers (x, out, codes, scales, amax, offs, workspaces) are
+ *     DEVICE pointers owned by the caller; the library never allocates, frees
+ *     or keeps them (fos_qdq_fused_static uses one fixed array of its own,
+ *     fos_mm a cuBLASLt handle per device).  Host-side arrays (the pointer /
+ *     size lists of the list calls) are read during the call only.
  *   - Tensors are row-major and contiguous: x is [rows, cols]; codes are
  *     [rows, cols/2] bytes, element 2j in the low nibble of byte j; scales are
  *     E4M3 bytes [rows, cols/16] (1x16) or [rows/16, cols/16] (16x16), plain
- *     row-major (no GEMM swizzle).
+ *     row-major (fos_swizzle_scales gives the tiled GEMM layout).
  *   - cols % 16 == 0; with 16x16 blocks also rows % 16 == 0.
  *   - x / out must be 32-byte aligned, codes 8-byte aligned (any row slice of
  *     a tensor from the CUDA caching allocator satisfies this).
  *   - Work is enqueued on `stream` of the device that owns the data and the
- *     call returns without synchronising the host.  The caller's current
- *     device is restored before return.
+ *     call returns without synchronising the host (fos_workspace_error, a
+ *     diagnostic, is the one exception).  The caller's current device is
+ *     restored before return.
  *   - Every argument is validated on the host before anything is launched;
  *     a failed check returns an error status and launches nothing.  CUDA
- *     launch failures return FOS_ERR_CUDA.  Kernels never trap and never
- *     wait on other work, so no call can hang the device.
+ *     launch failures return FOS_ERR_CUDA.  Kernels never trap.  The only
+ *     waits on other work are the bounded ones of fos_qdq_fused (between the
+ *     CTAs of its cooperative launch) and of the column-wise kernel (on its
+ *     own TMA loads); each gives up after about a second and reports it, so
+ *     no call can hang the device.
  *   - Global scale (reading of "FP32 global scale"): S = (6 * bound) / A,
  *     correctly rounded, for a global amax A; S = 1 when A is zero, negative,
  *     NaN or Inf; S = FLT_MAX when the quotient overflows.
