@@ -26,8 +26,8 @@
  *   - x / out must be 32-byte aligned, codes 8-byte aligned (any row slice of
  *     a tensor from the CUDA caching allocator satisfies this).
  *   - Work is enqueued on `stream` of the device that owns the data and the
- *     call returns without synchronising the host (fos_workspace_error, a
- *     diagnostic, is the one exception).  The caller's current device is
+ *     call returns without synchronising the host (fos_workspace_error and
+ *     fos_tile_amax_status, which read a result back, are the exceptions).  The caller's current device is
  *     restored before return.
  *   - Every argument is validated on the host before anything is launched;
  *     a failed check returns an error status and launches nothing.  CUDA
@@ -63,7 +63,9 @@ typedef enum {
     FOS_ERR_INVALID_ARG = 1, /* null pointer, negative size, bad enum value   */
     FOS_ERR_UNSUPPORTED = 2, /* shape / knob / dtype combination not offered  */
     FOS_ERR_MISALIGNED = 3,  /* pointer alignment rule above violated         */
-    FOS_ERR_CUDA = 4         /* a CUDA runtime call or launch failed          */
+    FOS_ERR_CUDA = 4,        /* a CUDA runtime call or launch failed          */
+    FOS_ERR_NONUNIFORM_TILE_AMAX = 5 /* fos_tile_amax_status: a 16-row tile's
+                                        per-row amax entries differ         */
 } fos_status;
 
 typedef enum { FOS_BF16 = 0, FOS_FP16 = 1, FOS_FP32 = 2 } fos_dtype;
@@ -125,6 +127,30 @@ FOS_API fos_status fos_amax(const void* x, fos_dtype dt, int64_t rows, int64_t c
 FOS_API fos_status fos_quantize(const void* x, fos_dtype dt, int64_t rows, int64_t cols,
                         const fos_config* cfg, float* amax, uint8_t* codes, uint8_t* scales,
                         fos_stream_t stream);
+
+/*
+ * fos_check_tile_amax -- validation of the tile-uniform contract above
+ * (grouped PR: with 16x16 blocks a row-scaled global scale must be the same
+ * for the 16 rows of a tile, so the per-row amax must be): counts the 16-row
+ * tiles of amax [rows] whose 16 entries are not all bitwise equal and writes
+ * the count to *bad (device int64, cleared by the call).  rows % 16 == 0;
+ * amax 4-byte aligned.  Asynchronous like every call; fos_quantize itself
+ * never checks (it uses each tile's first-row amax), so a caller that wants
+ * the check runs this first.  Errors: FOS_ERR_INVALID_ARG (null pointer with
+ * rows > 0, negative rows), FOS_ERR_UNSUPPORTED (rows % 16 != 0),
+ * FOS_ERR_MISALIGNED.
+ */
+FOS_API fos_status fos_check_tile_amax(const float* amax, int64_t rows, int64_t* bad,
+                                       fos_stream_t stream);
+
+/*
+ * fos_tile_amax_status -- the validating read of that count: waits for
+ * `stream`, reads *bad and returns FOS_OK when it is zero and
+ * FOS_ERR_NONUNIFORM_TILE_AMAX otherwise (FOS_ERR_INVALID_ARG for a pointer
+ * that is not device memory, FOS_ERR_CUDA when the wait fails).  This call
+ * synchronises the host.
+ */
+FOS_API fos_status fos_tile_amax_status(const int64_t* bad, fos_stream_t stream);
 
 /*
  * fos_quantize_list -- fos_quantize over a list of n tensors of one dtype

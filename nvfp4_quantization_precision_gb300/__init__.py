@@ -8,6 +8,7 @@ is not built, or a tensor is not on a CUDA device, the call raises.
 Entry points (names follow the C ABI):
   amax(x, granularity)                      -> float32 amax
   quantize(x, ...)                          -> (codes, scales, amax)
+  check_tile_amax(amax)                     -> number of non-uniform 16-row tiles
   quantize_list(xs, ...)                    -> ([codes], [scales], [amax])
   quantize_overlap(x, amax, codes, scales, x_next, amax_next)
   dequantize(codes, scales, amax, ...)      -> tensor
@@ -23,7 +24,8 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libfos.so")
 
-FOS_OK, FOS_ERR_INVALID_ARG, FOS_ERR_UNSUPPORTED, FOS_ERR_MISALIGNED, FOS_ERR_CUDA = range(5)
+(FOS_OK, FOS_ERR_INVALID_ARG, FOS_ERR_UNSUPPORTED, FOS_ERR_MISALIGNED, FOS_ERR_CUDA,
+ FOS_ERR_NONUNIFORM_TILE_AMAX) = range(6)
 FOS_BF16, FOS_FP16, FOS_FP32 = 0, 1, 2
 QDQ_MAX_LIST = 64
 GROUPED_MAX_GROUPS = 8192
@@ -89,7 +91,9 @@ def lib():
         L.fos_qdq_fused_workspace_bytes.restype = ctypes.c_size_t
         L.fos_qdq_fused.argtypes = [I, P, P, P, P, P, I, CFG, P, ctypes.c_size_t, P]
         L.fos_workspace_error.argtypes = [P, P, ctypes.POINTER(I)]
-        for n in ("fos_amax", "fos_quantize", "fos_quantize_list", "fos_quantize_overlap",
+        L.fos_check_tile_amax.argtypes = [P, I64, P, P]
+        L.fos_tile_amax_status.argtypes = [P, P]
+        for n in ("fos_check_tile_amax", "fos_tile_amax_status", "fos_amax", "fos_quantize", "fos_quantize_list", "fos_quantize_overlap",
                   "fos_dequantize", "fos_qdq", "fos_qdq_fused", "fos_workspace_error",
                   "fos_quantize_grouped", "fos_diag_convert"):
             getattr(L, n).restype = ctypes.c_int
@@ -140,15 +144,37 @@ def scales_shape(rows, cols, block16x16):
     return (rows // 16 if block16x16 else rows, cols // 16)
 
 
-def quantize(x, cfg=Config(), amax=None, codes=None, scales=None, amax_given=None):
+def check_tile_amax(amax, bad=None):
+    """Number of 16-row tiles of a per-row amax [rows] whose entries are not
+    all bitwise equal (fos_check_tile_amax); reads the count back, so it
+    waits for the stream."""
+    _cuda(amax, "amax")
+    if bad is None:
+        bad = torch.empty(1, dtype=torch.int64, device=amax.device)
+    _check(lib().fos_check_tile_amax(_p(amax), amax.numel(), _p(bad), _stream(amax)),
+           "fos_check_tile_amax")
+    return int(bad.item())
+
+
+def quantize(x, cfg=Config(), amax=None, codes=None, scales=None, amax_given=None,
+             validate=False):
     """Quantize x [rows, cols] (bf16 / fp16 / fp32).  amax is read when
     given (the default when a tensor is passed); with amax_given=False it is
     an output buffer the library fills.  With amax=None it is allocated,
-    computed and returned."""
+    computed and returned.  validate=True checks a given per-row amax of a
+    16x16 quantize for tile uniformity first (fos_check_tile_amax and
+    fos_tile_amax_status, which wait for the stream) and raises FosError
+    with FOS_ERR_NONUNIFORM_TILE_AMAX when a tile's rows differ."""
     _cuda(x, "x")
     R, C = x.shape
     dev = x.device
     given = (amax is not None) if amax_given is None else bool(amax_given)
+    if validate and given and cfg.block16x16 and cfg.row_scaled:
+        _cuda(amax, "amax")
+        bad = torch.empty(1, dtype=torch.int64, device=dev)
+        _check(lib().fos_check_tile_amax(_p(amax), amax.numel(), _p(bad), _stream(amax)),
+               "fos_check_tile_amax")
+        _check(lib().fos_tile_amax_status(_p(bad), _stream(amax)), "fos_quantize")
     if amax is None:
         amax = torch.empty(R if cfg.row_scaled else 1, dtype=torch.float32, device=dev)
     if codes is None:

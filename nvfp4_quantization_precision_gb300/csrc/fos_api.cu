@@ -373,6 +373,7 @@ const char* fos_status_string(fos_status s) {
         case FOS_ERR_UNSUPPORTED: return "unsupported shape, knob or dtype";
         case FOS_ERR_MISALIGNED: return "misaligned pointer";
         case FOS_ERR_CUDA: return "CUDA runtime error";
+        case FOS_ERR_NONUNIFORM_TILE_AMAX: return "per-row amax not uniform inside a 16-row tile";
     }
     return "unknown status";
 }
@@ -872,3 +873,35 @@ fos_status fos_mm(const uint8_t* a_codes, const uint8_t* a_scales_tiled, const f
 
 }  // extern "C"
 
+// ------------------------------------------------------------ tile-uniform amax check
+extern "C" {
+
+fos_status fos_check_tile_amax(const float* amax, int64_t rows, int64_t* bad,
+                               fos_stream_t stream) {
+    if (rows < 0 || !bad) return FOS_ERR_INVALID_ARG;
+    if (rows % 16 != 0) return FOS_ERR_UNSUPPORTED;
+    if (rows > 0 && !amax) return FOS_ERR_INVALID_ARG;
+    if (!aligned(bad, 8) || (amax && !aligned(amax, 4))) return FOS_ERR_MISALIGNED;
+    const int dev = rows > 0 ? common_device({amax, bad}) : device_of(bad);
+    if (dev < 0) return FOS_ERR_INVALID_ARG;
+    DeviceScope scope(dev);
+    if (scope.st) return scope.st;
+    return cuda_status(launch_check_tile_amax(amax, rows, bad,
+                                              reinterpret_cast<cudaStream_t>(stream)));
+}
+
+fos_status fos_tile_amax_status(const int64_t* bad, fos_stream_t stream) {
+    if (!bad) return FOS_ERR_INVALID_ARG;
+    const int dev = device_of(bad);
+    if (dev < 0) return FOS_ERR_INVALID_ARG;
+    DeviceScope scope(dev);
+    if (scope.st) return scope.st;
+    fos_status st = cuda_status(cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)));
+    if (st) return st;
+    int64_t v = 0;
+    st = cuda_status(cudaMemcpy(&v, bad, sizeof(v), cudaMemcpyDeviceToHost));
+    if (st) return st;
+    return v == 0 ? FOS_OK : FOS_ERR_NONUNIFORM_TILE_AMAX;
+}
+
+}  // extern "C"

@@ -129,5 +129,6 @@ int run_mm(const uint8_t* a_codes, const uint8_t* a_scales, const float* a_amax,
            int64_t N, int64_t K, float six_bound, float* out, int dev, cudaStream_t s);
 cudaError_t launch_swizzle(const uint8_t* scales, int64_t rows, int64_t nb, uint8_t* out,
                            cudaStream_t);
+cudaError_t launch_check_tile_amax(const float* amax, int64_t rows, int64_t* bad, cudaStream_t);
 
 }  // namespace fos

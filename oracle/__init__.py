@@ -246,6 +246,22 @@ def swizzle_scales(scales):
     return out
 
 
+def count_nonuniform_tiles(amax):
+    """The tile-uniform contract of 16x16 blocks with a row-scaled global
+    scale (grouped PR: the 16 rows of a tile share one amax): the number of
+    16-row tiles of a per-row amax [rows] whose 16 entries are not all
+    bitwise equal.  rows must be a multiple of 16."""
+    bits = np.ascontiguousarray(amax, dtype=np.float32).view(np.uint32).ravel()
+    if bits.size % 16:
+        raise ValueError("rows must be a multiple of 16")
+    count = 0
+    for t in range(bits.size // 16):
+        tile = bits[16 * t:16 * t + 16]
+        if any(int(v) != int(tile[0]) for v in tile):
+            count += 1
+    return count
+
+
 _OUTK = {"f32": (OUT_F32, np.float32), "bf16": (OUT_BF16, np.uint16), "f16": (OUT_F16, np.uint16)}
 
 

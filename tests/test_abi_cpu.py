@@ -246,3 +246,17 @@ def test_mm_rejects_before_any_cuda_call(L):
     assert call(a=None) == fos.FOS_ERR_INVALID_ARG
     assert call(a=ctypes.c_void_p(0x10008)) == fos.FOS_ERR_MISALIGNED
     assert call(M=0) == fos.FOS_OK
+
+
+def test_check_tile_amax_rejects_before_any_cuda_call(L):
+    i64 = ctypes.c_int64
+    assert "tile" in fos.status_string(fos.FOS_ERR_NONUNIFORM_TILE_AMAX)
+    assert L.fos_check_tile_amax(FAKE, i64(24), FAKE, None) == fos.FOS_ERR_UNSUPPORTED
+    assert L.fos_check_tile_amax(FAKE, i64(-16), FAKE, None) == fos.FOS_ERR_INVALID_ARG
+    assert L.fos_check_tile_amax(None, i64(16), FAKE, None) == fos.FOS_ERR_INVALID_ARG
+    assert L.fos_check_tile_amax(FAKE, i64(16), None, None) == fos.FOS_ERR_INVALID_ARG
+    assert L.fos_check_tile_amax(ctypes.c_void_p(0x10002), i64(16), FAKE,
+                                 None) == fos.FOS_ERR_MISALIGNED
+    assert L.fos_check_tile_amax(FAKE, i64(16), ctypes.c_void_p(0x10004),
+                                 None) == fos.FOS_ERR_MISALIGNED
+    assert L.fos_tile_amax_status(None, None) == fos.FOS_ERR_INVALID_ARG

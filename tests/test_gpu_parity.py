@@ -137,6 +137,53 @@ def test_16x16_row_amax_uses_first_tile_row():
     assert np.array_equal(gs.cpu().numpy(), os_) and np.array_equal(gc.cpu().numpy(), oc)
 
 
+
+@pytest.mark.parametrize("rows", [0, 16, 4096, 16 * 200003])
+def test_check_tile_amax_counts_like_the_oracle(rows):
+    """fos_check_tile_amax against the oracle's count on seeded per-row
+    amaxes: uniform tiles with a seeded set of tiles broken (a changed row,
+    a row of -0 in a tile of +0), over a grid larger than one pass."""
+    rng = np.random.default_rng(rows)
+    tiles = rows // 16
+    a = np.repeat(rng.uniform(0.5, 4.0, tiles).astype(np.float32), 16)
+    if tiles:
+        a[:16] = 0.0
+        broken = rng.choice(tiles, size=max(1, tiles // 7), replace=False)
+        for t in broken:
+            r = 16 * int(t) + int(rng.integers(16))
+            a[r] = -0.0 if a[r] == 0.0 else np.nextafter(a[r], np.float32(9))
+    want = oracle.count_nonuniform_tiles(a)
+    assert fos.check_tile_amax(torch.from_numpy(a).to(DEV)) == want
+    bad = torch.empty(1, dtype=torch.int64, device=DEV)
+    L = fos.lib()
+    assert L.fos_check_tile_amax(ctypes.c_void_p(torch.from_numpy(a).to(DEV).data_ptr()) if rows
+                                 else ctypes.c_void_p(0), ctypes.c_int64(rows),
+                                 ctypes.c_void_p(bad.data_ptr()), None) == fos.FOS_OK
+    assert L.fos_tile_amax_status(ctypes.c_void_p(bad.data_ptr()), None) == (
+        fos.FOS_OK if want == 0 else fos.FOS_ERR_NONUNIFORM_TILE_AMAX)
+
+
+def test_quantize_validate_rejects_a_nonuniform_tile_amax():
+    """quantize(validate=True) of 16x16 blocks with a given per-row amax:
+    raises FOS_ERR_NONUNIFORM_TILE_AMAX when one tile's rows differ and
+    writes nothing; with tile-uniform amax it equals the oracle."""
+    x = workloads.weight(64, 256, seed=5, dtype=torch.bfloat16)
+    xf = x.float().numpy()
+    gcfg, ocfg = _cfgs("mse", 448, True, b16=True)
+    a = np.repeat(oracle.amax_rows(xf).reshape(4, 16).max(axis=1), 16).astype(np.float32)
+    ocfg = oracle.Config(**{**ocfg.__dict__, "amax_is_input": True})
+    oc, os_, _ = oracle.quantize(xf, ocfg, amax=a)
+    gc, gs, _ = fos.quantize(x.to(DEV), gcfg, amax=torch.from_numpy(a).to(DEV), validate=True)
+    torch.cuda.synchronize()
+    assert np.array_equal(gs.cpu().numpy(), os_) and np.array_equal(gc.cpu().numpy(), oc)
+    a[37] *= 2
+    codes = torch.full((64, 128), 0x5A, dtype=torch.uint8, device=DEV)
+    with pytest.raises(fos.FosError) as e:
+        fos.quantize(x.to(DEV), gcfg, amax=torch.from_numpy(a).to(DEV), codes=codes,
+                     validate=True)
+    assert e.value.status == fos.FOS_ERR_NONUNIFORM_TILE_AMAX
+    assert bool((codes == 0x5A).all())
+
 # ------------------------------------------------------------------ special values
 def _special_tensor(dt):
     rng = np.random.default_rng(0)
@@ -722,6 +769,24 @@ def test_swizzle_scales(shape):
     assert np.array_equal(got.cpu().numpy(), oracle.swizzle_scales(s))
 
 
+
+@pytest.mark.parametrize("shape", [(300, 64), (130, 48)])
+def test_swizzle_scales_unaligned_pointers(shape):
+    """Scales that start one byte into a buffer and an output that starts 4
+    bytes into one take the byte-load and 4-byte-store forms of the kernel;
+    the bytes are those of the oracle's layout."""
+    R, C = shape
+    s = np.random.default_rng(R).integers(0, 0x7F, (R, C // 16), dtype=np.uint8)
+    src = torch.zeros(s.size + 16, dtype=torch.uint8, device=DEV)
+    src[1:1 + s.size] = torch.from_numpy(s.ravel()).to(DEV)
+    n = -(-R // 128) * 128 * (-(-(C // 16) // 4) * 4)
+    dst = torch.full((n + 16,), 0xEE, dtype=torch.uint8, device=DEV)
+    fos.swizzle_scales(src[1:1 + s.size], R, C, out=dst[4:4 + n])
+    torch.cuda.synchronize()
+    got = dst.cpu().numpy()
+    assert np.array_equal(got[4:4 + n], oracle.swizzle_scales(s))
+    assert (got[:4] == 0xEE).all() and (got[4 + n:] == 0xEE).all()
+
 @pytest.mark.parametrize("mode", ["std", "mse"])
 def test_swizzled_scales_feed_an_fp4_gemm(mode):
     """Codes and tiled scales from this library, handed to PyTorch's NVFP4
@@ -792,3 +857,45 @@ def test_mm_of_quantized_operands(mode, row):
     ref = D * ga * gb
     err = np.abs(out.cpu().numpy().astype(np.float64) - ref)
     assert np.all(err <= bound * np.abs(ga * gb) + 1e-30), float((err / (bound * np.abs(ga * gb) + 1e-30)).max())
+
+
+def _at16(t):
+    """A copy of t whose storage starts 16 bytes into a larger buffer: 16-byte
+    but not 256-byte aligned."""
+    nb = t.numel() * t.element_size()
+    buf = torch.zeros(nb + 256, dtype=torch.uint8, device=t.device)
+    v = buf[16:16 + nb].view(t.dtype).view(t.shape)
+    v.copy_(t)
+    return v
+
+
+def test_mm_in_row_chunks_with_16_byte_aligned_operands():
+    """A product whose fp32 output is larger than half the L2 runs as several
+    row-chunk GEMMs, each followed by its epilogue; operands and output
+    placed 16 bytes into their buffers.  Sampled rows of every chunk (and the
+    ragged last one), row-scaled a, against the oracle's block values within
+    the fp32 accumulation bound."""
+    M, N, K = 2176, 16384, 128
+    gcfg_a, ocfg_a = _cfgs("mse", 448, True)
+    gcfg_b, ocfg_b = _cfgs("mse", 448)
+    a = _x(M, K, "F4", 61, "bf16")
+    b = workloads.weight(N, K, seed=62, dtype=torch.bfloat16)
+    ca, sa, aa = fos.quantize(a.to(DEV), gcfg_a)
+    cb, sb, ab = fos.quantize(b.to(DEV), gcfg_b)
+    ta, tb = fos.swizzle_scales(sa, M, K), fos.swizzle_scales(sb, N, K)
+    out = _at16(torch.zeros((M, N), dtype=torch.float32, device=DEV))
+    got = fos.mm(_at16(ca), _at16(ta), aa, _at16(cb), _at16(tb), ab, gcfg_a, out=out)
+    torch.cuda.synchronize()
+    assert got.data_ptr() % 256 == 16
+    oca, osa, oaa = oracle.quantize(a.float().numpy(), ocfg_a)
+    ocb, osb, oab = oracle.quantize(b.float().numpy(), ocfg_b)
+    assert np.array_equal(ca.cpu().numpy(), oca) and np.array_equal(cb.cpu().numpy(), ocb)
+    rows = np.unique(np.concatenate([np.arange(0, M, 97), [M - 1, M - 16, 767, 768, 1536]]))
+    pa, pb = _block_values(oca[rows], osa[rows]), _block_values(ocb, osb)
+    ga = (1.0 / np.array([oracle.global_scale(float(v), 448) for v in oaa[rows]],
+                         np.float32)).reshape(-1, 1)
+    gb = 1.0 / np.float32(oracle.global_scale(float(oab[0]), 448))
+    ref = (pa @ pb.T) * ga * gb
+    bound = (K + 2) * 2.0 ** -24 * (np.abs(pa) @ np.abs(pb).T) * np.abs(ga * gb)
+    err = np.abs(got.cpu().numpy()[rows].astype(np.float64) - ref)
+    assert np.all(err <= bound + 1e-30), float((err / (bound + 1e-30)).max())

@@ -564,3 +564,25 @@ def test_swizzled_scale_layout_offsets(orc):
     # a bijection on the padded matrix: every byte of a distinct-valued input appears once
     vals = (full % 251 + 1).astype(np.uint8)
     assert np.array_equal(np.sort(orc.swizzle_scales(vals)), np.sort(vals.ravel()))
+
+
+def test_tile_uniform_count_hand_cases(orc):
+    """The tile-uniform contract of 16x16 blocks with row-scaled amax
+    (grouped PR): counts built by hand.  Equal rows give 0; one differing
+    row, two differing rows in one tile, and +0 against -0 (bitwise reading)
+    each add one tile."""
+    a = np.ones(96, np.float32)
+    assert orc.count_nonuniform_tiles(a) == 0
+    a[17] = 2.0                      # tile 1
+    assert orc.count_nonuniform_tiles(a) == 1
+    a[40] = 3.0
+    a[47] = 3.0                      # tile 2, two rows
+    assert orc.count_nonuniform_tiles(a) == 2
+    a[48:64] = 0.0
+    a[63] = -0.0                     # tile 3: equal as floats, not as bits
+    assert orc.count_nonuniform_tiles(a) == 3
+    a[0] = 5.0                       # tile 0, first row differs from the rest
+    assert orc.count_nonuniform_tiles(a) == 4
+    assert orc.count_nonuniform_tiles(np.zeros(0, np.float32)) == 0
+    with pytest.raises(ValueError):
+        orc.count_nonuniform_tiles(np.ones(17, np.float32))
