@@ -11,8 +11,9 @@
 namespace fos {
 
 // out[m][n] = (D[m][n] * g_a(m)) * g_b, g = rn(1 / S) of the global scale S
-// that quantization used (per row of a when row-scaled).  Four elements per
-// thread (N is a multiple of 16).
+// that quantization used (per row of a when row-scaled).  A CTA takes whole
+// rows (one g_a each), its threads four columns at a time (N is a multiple
+// of 16).
 __global__ void __launch_bounds__(kThreads) k_mm_epilogue(float* out, const float* a_amax,
                                                          int a_row, const float* b_amax,
                                                          int64_t M, int64_t N, float six_bound) {
@@ -20,17 +21,18 @@ __global__ void __launch_bounds__(kThreads) k_mm_epilogue(float* out, const floa
     chain_release();
     const float gb = fdiv(1.0f, global_scale(b_amax[0], six_bound));
     const float ga0 = a_row ? 0.0f : fdiv(1.0f, global_scale(a_amax[0], six_bound));
-    const int64_t quads = M * (N / 4);
-    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    for (int64_t q = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; q < quads; q += stride) {
-        const int64_t m = q / (N / 4);
+    const int64_t nq = N / 4;
+    for (int64_t m = blockIdx.x; m < M; m += gridDim.x) {
         const float ga = a_row ? fdiv(1.0f, global_scale(a_amax[m], six_bound)) : ga0;
-        float4 v = reinterpret_cast<float4*>(out)[q];
-        v.x = fmul(fmul(v.x, ga), gb);
-        v.y = fmul(fmul(v.y, ga), gb);
-        v.z = fmul(fmul(v.z, ga), gb);
-        v.w = fmul(fmul(v.w, ga), gb);
-        reinterpret_cast<float4*>(out)[q] = v;
+        float4* row = reinterpret_cast<float4*>(out + m * N);
+        for (int64_t q = threadIdx.x; q < nq; q += blockDim.x) {
+            float4 v = row[q];
+            v.x = fmul(fmul(v.x, ga), gb);
+            v.y = fmul(fmul(v.y, ga), gb);
+            v.z = fmul(fmul(v.z, ga), gb);
+            v.w = fmul(fmul(v.w, ga), gb);
+            row[q] = v;
+        }
     }
 }
 
@@ -47,16 +49,23 @@ static cublasLtHandle_t lt_handle(int dev) {
     return h;
 }
 
-// 0: done; 1: the library offers no algorithm for this shape; 2: a cuBLASLt
-// or CUDA call failed.
-int run_mm(const uint8_t* a_codes, const uint8_t* a_scales, const float* a_amax, int a_row,
-           const uint8_t* b_codes, const uint8_t* b_scales, const float* b_amax, int64_t M,
-           int64_t N, int64_t K, float six_bound, float* out, int dev, cudaStream_t s) {
-    cublasLtHandle_t h = lt_handle(dev);
-    if (!h) return 2;
-    // Column-major view: D (N x M, ld N) = op(A') (N x K) * op(B') (K x M), with
-    // A' = b's codes as K x N (each column one row of b, K contiguous; op = T)
-    // and B' = a's codes as K x M (op = N); D column-major is out row-major.
+// Largest power of two (at most 256) that divides the address.
+static uint32_t align_of(const void* p) {
+    const uintptr_t v = reinterpret_cast<uintptr_t>(p);
+    uint32_t a = 256;
+    while (a > 1 && (v & (a - 1))) a >>= 1;
+    return a;
+}
+
+// One block-scaled GEMM of `mrows` rows of a (codes, tiled scales) against
+// all of b into out[mrows, N].  0: done; 1: no algorithm; 2: a call failed.
+static int lt_gemm(cublasLtHandle_t h, const uint8_t* a_codes, const uint8_t* a_scales,
+                   const uint8_t* b_codes, const uint8_t* b_scales, int64_t mrows, int64_t N,
+                   int64_t K, float* out, cudaStream_t s) {
+    // Column-major view: D (N x mrows, ld N) = op(A') (N x K) * op(B') (K x mrows),
+    // with A' = b's codes as K x N (each column one row of b, K contiguous;
+    // op = T) and B' = a's codes as K x mrows (op = N); D column-major is out
+    // row-major.
     cublasLtMatmulDesc_t op = nullptr;
     cublasLtMatrixLayout_t la = nullptr, lb = nullptr, ld = nullptr;
     cublasLtMatmulPreference_t pref = nullptr;
@@ -80,13 +89,23 @@ int run_mm(const uint8_t* a_codes, const uint8_t* a_scales, const float* a_amax,
                                            sizeof(sb)))
             break;
         if (cublasLtMatrixLayoutCreate(&la, CUDA_R_4F_E2M1, K, N, K) ||
-            cublasLtMatrixLayoutCreate(&lb, CUDA_R_4F_E2M1, K, M, K) ||
-            cublasLtMatrixLayoutCreate(&ld, CUDA_R_32F, N, M, N))
+            cublasLtMatrixLayoutCreate(&lb, CUDA_R_4F_E2M1, K, mrows, K) ||
+            cublasLtMatrixLayoutCreate(&ld, CUDA_R_32F, N, mrows, N))
             break;
         if (cublasLtMatmulPreferenceCreate(&pref)) break;
         const size_t ws = 0;
+        // the heuristic assumes 256-byte aligned buffers unless told otherwise
+        const uint32_t al_a = align_of(b_codes), al_b = align_of(a_codes), al_d = align_of(out);
         if (cublasLtMatmulPreferenceSetAttribute(pref, CUBLASLT_MATMUL_PREF_MAX_WORKSPACE_BYTES,
-                                                 &ws, sizeof(ws)))
+                                                 &ws, sizeof(ws)) ||
+            cublasLtMatmulPreferenceSetAttribute(pref, CUBLASLT_MATMUL_PREF_MIN_ALIGNMENT_A_BYTES,
+                                                 &al_a, sizeof(al_a)) ||
+            cublasLtMatmulPreferenceSetAttribute(pref, CUBLASLT_MATMUL_PREF_MIN_ALIGNMENT_B_BYTES,
+                                                 &al_b, sizeof(al_b)) ||
+            cublasLtMatmulPreferenceSetAttribute(pref, CUBLASLT_MATMUL_PREF_MIN_ALIGNMENT_C_BYTES,
+                                                 &al_d, sizeof(al_d)) ||
+            cublasLtMatmulPreferenceSetAttribute(pref, CUBLASLT_MATMUL_PREF_MIN_ALIGNMENT_D_BYTES,
+                                                 &al_d, sizeof(al_d)))
             break;
         cublasLtMatmulHeuristicResult_t res = {};
         int found = 0;
@@ -99,13 +118,7 @@ int run_mm(const uint8_t* a_codes, const uint8_t* a_scales, const float* a_amax,
         if (cublasLtMatmul(h, op, &alpha, b_codes, la, a_codes, lb, &beta, out, ld, out, ld,
                            &res.algo, nullptr, 0, s))
             break;
-        int64_t quads = M * (N / 4);
-        int64_t blocks = (quads + kThreads - 1) / kThreads;
-        const int64_t cap = (int64_t)sm_count() * 8;
-        if (blocks > cap) blocks = cap;
-        k_mm_epilogue<<<(unsigned)blocks, kThreads, 0, s>>>(out, a_amax, a_row, b_amax, M, N,
-                                                            six_bound);
-        rc = cudaGetLastError() == cudaSuccess ? 0 : 2;
+        rc = 0;
     } while (false);
     if (pref) cublasLtMatmulPreferenceDestroy(pref);
     if (ld) cublasLtMatrixLayoutDestroy(ld);
@@ -113,6 +126,45 @@ int run_mm(const uint8_t* a_codes, const uint8_t* a_scales, const float* a_amax,
     if (la) cublasLtMatrixLayoutDestroy(la);
     if (op) cublasLtMatmulDescDestroy(op);
     return rc;
+}
+
+// Rows of a per GEMM: a multiple of 256 whose fp32 output slice takes about
+// half of the L2, so that the epilogue that follows each GEMM reads D back
+// from L2 instead of HBM; all of M when it fits.
+static int64_t chunk_rows(int64_t M, int64_t N, int dev) {
+    int l2 = 0;
+    if (cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return M;
+    }
+    int64_t mc = (int64_t)l2 / 2 / (N * 4) / 256 * 256;
+    if (mc < 256) mc = 256;
+    return mc >= M ? M : mc;
+}
+
+// 0: done; 1: the library offers no algorithm for this shape; 2: a cuBLASLt
+// or CUDA call failed.
+int run_mm(const uint8_t* a_codes, const uint8_t* a_scales, const float* a_amax, int a_row,
+           const uint8_t* b_codes, const uint8_t* b_scales, const float* b_amax, int64_t M,
+           int64_t N, int64_t K, float six_bound, float* out, int dev, cudaStream_t s) {
+    cublasLtHandle_t h = lt_handle(dev);
+    if (!h) return 2;
+    const int64_t mc = chunk_rows(M, N, dev);
+    // a's tiled scales: 128-row tile rows of 128 * (K / 16) bytes (K % 64 == 0),
+    // so a chunk that starts on a multiple of 128 rows starts at m0 * K / 16.
+    for (int64_t m0 = 0; m0 < M; m0 += mc) {
+        const int64_t rows = (M - m0 < mc) ? (M - m0) : mc;
+        const int rc = lt_gemm(h, a_codes + m0 * (K / 2), a_scales + m0 * (K / 16), b_codes,
+                               b_scales, rows, N, K, out + m0 * N, s);
+        if (rc) return rc;
+        int64_t blocks = rows;
+        const int64_t cap = (int64_t)sm_count() * 8;
+        if (blocks > cap) blocks = cap;
+        k_mm_epilogue<<<(unsigned)blocks, kThreads, 0, s>>>(
+            out + m0 * N, a_amax + (a_row ? m0 : 0), a_row, b_amax, rows, N, six_bound);
+        if (cudaGetLastError() != cudaSuccess) return 2;
+    }
+    return 0;
 }
 
 }  // namespace fos
