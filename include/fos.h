@@ -230,7 +230,9 @@ FOS_API fos_status fos_swizzle_scales(const uint8_t* scales, int64_t rows, int64
  * cuBLASLt NVFP4 GEMM (a library GEMM: fp32 accumulation, no workspace);
  * this library's epilogue then applies the global decode scales,
  *   out[m][n] = (D[m][n] * g_a(m)) * g_b,  g = rn(1 / S),
- * S the global scale fos_quantize used (cfg->e4m3_bound).  out: fp32 [M, N]
+ * S the global scale fos_quantize used (cfg->e4m3_bound).  Large products
+ * run as several GEMMs over row chunks of a, each followed by the epilogue
+ * while its output is still in L2.  out: fp32 [M, N]
  * row-major, 16-byte aligned, like all operands.  M and N multiples of 16,
  * K a multiple of 64; FOS_ERR_UNSUPPORTED when cuBLASLt offers no
  * algorithm.  The first call on a device creates its cuBLASLt handle.
