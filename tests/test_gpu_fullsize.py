@@ -190,3 +190,63 @@ def test_mm_full_size_sampled():
     bound = (K + 2) * 2.0 ** -24 * (np.abs(pa) @ np.abs(pw).T) * abs(g)
     got = out.cpu().numpy()[np.ix_(ra, rw)].astype(np.float64)
     assert np.all(np.abs(got - ref) <= bound + 1e-30)
+
+
+def test_past_2_to_31_elements_sampled():
+    """A bf16 tensor of 524352 x 4096 = 2^31 + 2^18 elements (element 2^31 is
+    row 524288, column 0), amax 5.0 by construction: the per-tensor and
+    per-row 1x16 quantize, the 16x16 quantize, the dequantize, the fused QDQ
+    and the column-wise operand, each on rows (or columns) on both sides of
+    the 2^31 boundary and at the end, against the oracle bit for bit."""
+    R, C = 524352, 4096
+    x = workloads.large_activation(R, C, seed=3, device=DEV)
+    rows = np.array([0, 1, 524272, 524287, 524288, 524289, 524303, R - 16, R - 1])
+    ridx = torch.from_numpy(rows).to(DEV)
+    xs = x[ridx].cpu().float().numpy()
+    five = np.array([5.0], np.float32)
+    given = oracle.Config(amax_is_input=True)
+
+    codes, scales, amax = fos.quantize(x, fos.Config())
+    torch.cuda.synchronize()
+    assert np.array_equal(_u32(amax), five.view(np.uint32))
+    oc, os_, _ = oracle.quantize(xs, given, amax=five)
+    assert np.array_equal(codes[ridx].cpu().numpy(), oc)
+    assert np.array_equal(scales[ridx].cpu().numpy(), os_)
+    deq = fos.dequantize(codes, scales, amax, fos.Config(), out_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    od = oracle.dequantize(oc, os_, five, given, "bf16")
+    assert np.array_equal(_u16(deq[ridx]), od)
+    del codes, scales, deq
+
+    out = fos.qdq([x], fos.Config(), amaxes=[amax])[0]
+    torch.cuda.synchronize()
+    oq, _ = oracle.qdq(xs, given, "bf16", amax=five)
+    assert np.array_equal(_u16(out[ridx]), oq)
+    del out
+
+    rc, rs, ra = fos.quantize(x, fos.Config(row_scaled=True))
+    torch.cuda.synchronize()
+    orc_, ors, ora = oracle.quantize(xs, oracle.Config(row_scaled=True))
+    assert np.array_equal(_u32(ra[ridx]), ora.view(np.uint32))
+    assert np.array_equal(rc[ridx].cpu().numpy(), orc_)
+    assert np.array_equal(rs[ridx].cpu().numpy(), ors)
+    del rc, rs, ra
+
+    bands = np.array([0, 524288 // 16 - 1, 524288 // 16, R // 16 - 1])
+    brows = torch.from_numpy(_band_rows(bands)).to(DEV)
+    tc, ts, _ = fos.quantize(x, fos.Config(block16x16=True), amax=amax)
+    torch.cuda.synchronize()
+    otc, ots, _ = oracle.quantize(x[brows].cpu().float().numpy(),
+                                  oracle.Config(block16x16=True, amax_is_input=True), amax=five)
+    assert np.array_equal(tc[brows].cpu().numpy(), otc)
+    assert np.array_equal(ts[torch.from_numpy(bands).to(DEV)].cpu().numpy(), ots)
+    del tc, ts
+
+    cols = np.array([0, 2047, C - 2, C - 1])
+    ct, st, _ = fos.quantize_colwise(x, fos.Config(), amax=amax)
+    torch.cuda.synchronize()
+    xc = x[:, torch.from_numpy(cols).to(DEV)].cpu().float().numpy()
+    octc, octs, _ = oracle.quantize_colwise(xc, given, amax=five)
+    cidx = torch.from_numpy(cols).to(DEV)
+    assert np.array_equal(ct[cidx].cpu().numpy(), octc)
+    assert np.array_equal(st[cidx].cpu().numpy(), octs)

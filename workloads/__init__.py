@@ -11,6 +11,8 @@ Families (activation rows, 1x16 blocks along the last axis):
   F3  U(-1, 1)
   F4  N(0, 1) with 25 % of the 16-element row blocks replaced: one third all
       zero (half +0, half -0), one third scaled by 1e-4, one third by 1e-7
+Large activation (past 2^31 elements): N(0, 1) clipped to [-4, 4] plus one
+planted 5.0, so that its amax is known without reading it.
 Weights: N(0, 0.02) with 0.05 % of entries x50.
 Fake-QAT weight list: N(0, 0.02) with 0.1 % of entries x30.
 MoE: token-group sizes ~ round(lognormal(0, 1)) scaled to about 94 % of the
@@ -121,6 +123,20 @@ def moe_experts(experts, rows, cols, seed=0, dtype=torch.bfloat16, device="cpu")
     f = torch.exp(0.5 * torch.randn(experts, generator=gc, dtype=torch.float32))
     x *= f.to(device).view(experts, 1, 1)
     return _finish(x, dtype)
+
+
+def large_activation(rows, cols, seed=0, dtype=torch.bfloat16, device="cpu", chunk_rows=65536):
+    """N(0, 1) clipped to [-4, 4], drawn in row chunks of float32 (so a tensor
+    of several GB needs little staging), with one planted 5.0 in the last
+    element: the tensor amax is 5.0 by construction."""
+    g = _gen(seed, device)
+    x = torch.empty(rows, cols, dtype=dtype, device=device)
+    for r0 in range(0, rows, chunk_rows):
+        r1 = min(rows, r0 + chunk_rows)
+        x[r0:r1] = _finish(torch.randn(r1 - r0, cols, generator=g, device=device,
+                                       dtype=torch.float32).clamp_(-4.0, 4.0), dtype)
+    x[rows - 1, cols - 1] = 5.0
+    return x
 
 
 def ceil_div(a, b):
