@@ -144,7 +144,26 @@ __global__ void __launch_bounds__(kThreads, min_ctas<EM>()) k_quant1x16_tensor(c
     const float S = global_scale(a.amax[0], a.six_bound);
     build_table(tbl, S, lane);
     uint32_t dummy[8];
-    for (int64_t b = b0; b < a.nblk + lane; b += kBuf * step) {  // b - lane: first block of unit
+    // Steady state: while every unit this step loads or encodes is whole
+    // (the test is on the unit's first block, the same for the whole warp),
+    // loads and encodes go without bounds checks or branches; the guarded
+    // loop below finishes the tail.
+    int64_t b = b0;
+    for (; b - lane + (2 * kBuf - 2) * step + 31 < a.nblk; b += kBuf * step) {
+#pragma unroll
+        for (int k = 0; k < kBuf; ++k) {
+            load_seg<IT, kEncHint>(buf[(k + kBuf - 1) % kBuf],
+                                   xb + (b + (k + kBuf - 1) * step) * kBytes);
+            uint64_t xp[8];
+            widen<IT>(buf[k], xp);
+            uint32_t code[2], scale;
+            const int64_t bc = b + k * step;
+            encode_block<EM, Out::NONE>(xp, S, tbl, nz, code, scale, dummy);
+            st64(a.codes + bc * 8, code[0], code[1]);
+            st8(a.scales + bc, scale);
+        }
+    }
+    for (; b < a.nblk + lane; b += kBuf * step) {  // b - lane: first block of unit
 #pragma unroll
         for (int k = 0; k < kBuf; ++k) {
             const int64_t bl = b + (k + kBuf - 1) * step;  // unit loaded now
@@ -805,7 +824,40 @@ __global__ void __launch_bounds__(kThreads, tile_min_ctas<IT>()) k_quant16x16(co
         S = global_scale(a.amax[0], a.six_bound);
         build_table(tbl, S, lane);
     }
-    for (int64_t u = u0; u < c1; u += ustep) {
+    int64_t u = u0;
+    if constexpr (kGrid) {
+        // Steady state (every quad of a band whole, the next unit in range):
+        // loads and stores without bounds checks or zero fill.
+        if ((a.nb & 3) == 0) {
+            for (; u + ustep < c1; u += ustep) {
+                RowChunk nc = cc;
+                nc.row += step_rows;
+                nc.chunk += step_chunks;
+                if (nc.chunk >= a.cpr) {
+                    nc.chunk -= a.cpr;
+                    ++nc.row;
+                }
+                const char* q = xb + ((nc.row * 16 + r) * cols + (nc.chunk * 4 + t) * 16) * kElt;
+                Raw<IT> nxt0, nxt1;
+                load_seg<IT, kEncHint>(nxt0, q);
+                load_seg<IT, kEncHint>(nxt1, q + 8 * cols * kElt);
+                const int64_t J = cc.chunk * 4 + t;
+                uint8_t* c0 = a.codes + (cc.row * 16 + r) * (cols / 2) + J * 8;
+                uint64_t x0[8], x1[8];
+                widen<IT>(cur0, x0);
+                widen<IT>(cur1, x1);
+                uint32_t k0[2], k1[2], scale;
+                encode_tile_rows<EM>(x0, x1, S, tbl, nz, t, k0, k1, scale);
+                st64(c0, k0[0], k0[1]);
+                st64(c0 + 8 * (cols / 2), k1[0], k1[1]);
+                if (r == 0) st8(a.scales + cc.row * a.nb + J, scale);
+                cur0 = nxt0;
+                cur1 = nxt1;
+                cc = nc;
+            }
+        }
+    }
+    for (; u < c1; u += ustep) {
         RowChunk nc = cc;  // this warp's next unit, ustep units on
         nc.row += step_rows;
         nc.chunk += step_chunks;
