@@ -213,13 +213,8 @@ __global__ void __launch_bounds__(kThreads, min_ctas<EM>()) k_quant1x16(const En
     int64_t key = -1;
     float S = 1.0f;
     uint32_t dummy[8];
+    const bool whole_chunks = (a.nb & 31) == 0;
     for (int64_t u = u0; u < u1; ++u) {
-        RowChunk nc = cc;
-        nc.next(a.cpr);
-        const int64_t jn = nc.chunk * 32 + lane;
-        Raw<IT> nxt;
-        load_if<IT, kEncHint>(nxt, xb + (nc.row * a.nb + jn) * kBytes,
-                    u + 1 < u1 && jn < a.nb && nc.row < last_end);
         int64_t k;
         if constexpr (SRC == Src::ROW) {
             k = cc.row;
@@ -234,6 +229,35 @@ __global__ void __launch_bounds__(kThreads, min_ctas<EM>()) k_quant1x16(const En
                 build_table(tbl, S, lane);
             }
         }
+        if (whole_chunks && (SRC == Src::ROW || k < a.G)) {
+            // steady state: the next unit is whole and under the same scale
+            const int64_t seg_end = (SRC == Src::ROW) ? cc.row + 1 : (int64_t)s_ends[k];
+            while (u + 1 < u1) {
+                RowChunk nc = cc;
+                nc.next(a.cpr);
+                if (nc.row >= seg_end) break;
+                const int64_t jn = nc.chunk * 32 + lane;
+                Raw<IT> nxt;
+                load_seg<IT, kEncHint>(nxt, xb + (nc.row * a.nb + jn) * kBytes);
+                uint64_t xp[8];
+                widen<IT>(cur, xp);
+                uint32_t code[2], scale;
+                encode_block<EM, Out::NONE>(xp, S, tbl, nz, code, scale, dummy);
+                const int64_t b = cc.row * a.nb + j;
+                st64(a.codes + b * 8, code[0], code[1]);
+                st8(a.scales + b, scale);
+                cur = nxt;
+                cc = nc;
+                j = jn;
+                ++u;
+            }
+        }
+        RowChunk nc = cc;
+        nc.next(a.cpr);
+        const int64_t jn = nc.chunk * 32 + lane;
+        Raw<IT> nxt;
+        load_if<IT, kEncHint>(nxt, xb + (nc.row * a.nb + jn) * kBytes,
+                    u + 1 < u1 && jn < a.nb && nc.row < last_end);
         const int64_t b = cc.row * a.nb + j;
         if (j < a.nb) {
             if (cc.row < last_end) {
@@ -825,11 +849,33 @@ __global__ void __launch_bounds__(kThreads, tile_min_ctas<IT>()) k_quant16x16(co
         build_table(tbl, S, lane);
     }
     int64_t u = u0;
-    if constexpr (kGrid) {
-        // Steady state (every quad of a band whole, the next unit in range):
-        // loads and stores without bounds checks or zero fill.
-        if ((a.nb & 3) == 0) {
-            for (; u + ustep < c1; u += ustep) {
+    const bool quads_whole = (a.nb & 3) == 0;  // every band is whole tile quads
+    for (; u < c1; u += ustep) {
+        bool tail = false;
+        int64_t seg_end = INT64_MAX;  // first band past the current scale's segment
+        if constexpr (SRC != Src::TENSOR) {
+            int64_t k;
+            if constexpr (SRC == Src::ROW) {
+                k = cc.row * 16;  // a tile uses the amax of its first row
+                seg_end = cc.row + 1;
+            } else {
+                while (g < a.G && cc.row * 16 >= s_ends[g]) ++g;
+                k = g;
+                tail = (g >= a.G);
+                if (!tail) seg_end = ((int64_t)s_ends[g] + 15) / 16;
+            }
+            if (k != key) {
+                key = k;
+                if (!tail) {
+                    S = global_scale(a.amax[k], a.six_bound);
+                    build_table(tbl, S, lane);
+                }
+            }
+        }
+        if (quads_whole && !tail) {
+            // Steady state: while the next unit lies whole under the same
+            // scale, loads and stores go without bounds checks or zero fill.
+            while (u + ustep < c1) {
                 RowChunk nc = cc;
                 nc.row += step_rows;
                 nc.chunk += step_chunks;
@@ -837,6 +883,7 @@ __global__ void __launch_bounds__(kThreads, tile_min_ctas<IT>()) k_quant16x16(co
                     nc.chunk -= a.cpr;
                     ++nc.row;
                 }
+                if (nc.row >= seg_end) break;
                 const char* q = xb + ((nc.row * 16 + r) * cols + (nc.chunk * 4 + t) * 16) * kElt;
                 Raw<IT> nxt0, nxt1;
                 load_seg<IT, kEncHint>(nxt0, q);
@@ -854,10 +901,9 @@ __global__ void __launch_bounds__(kThreads, tile_min_ctas<IT>()) k_quant16x16(co
                 cur0 = nxt0;
                 cur1 = nxt1;
                 cc = nc;
+                u += ustep;
             }
         }
-    }
-    for (; u < c1; u += ustep) {
         RowChunk nc = cc;  // this warp's next unit, ustep units on
         nc.row += step_rows;
         nc.chunk += step_chunks;
@@ -868,24 +914,6 @@ __global__ void __launch_bounds__(kThreads, tile_min_ctas<IT>()) k_quant16x16(co
         Raw<IT> nxt0, nxt1;
         load_unit(nxt0, nxt1, nc, u + ustep < c1);
         const int64_t band = cc.row;
-        bool tail = false;
-        if constexpr (SRC != Src::TENSOR) {
-            int64_t k;
-            if constexpr (SRC == Src::ROW) {
-                k = band * 16;  // a tile uses the amax of its first row
-            } else {
-                while (g < a.G && band * 16 >= s_ends[g]) ++g;
-                k = g;
-                tail = (g >= a.G);
-            }
-            if (k != key) {
-                key = k;
-                if (!tail) {
-                    S = global_scale(a.amax[k], a.six_bound);
-                    build_table(tbl, S, lane);
-                }
-            }
-        }
         const int64_t J = cc.chunk * 4 + t;
         uint8_t* c0 = a.codes + (band * 16 + r) * (cols / 2) + J * 8;
         uint8_t* c8 = c0 + 8 * (cols / 2);
