@@ -13,7 +13,12 @@ Entry points (names follow the C ABI):
   quantize_overlap(x, amax, codes, scales, x_next, amax_next)
   dequantize(codes, scales, amax, ...)      -> tensor
   qdq(xs, ...)                              -> list of tensors (one launch)
+  qdq_fused(xs, ...)                        -> (outs, amaxes), every amax in the same launch
+  workspace_error(workspace)                -> error word of a fused launch
   quantize_grouped(x, offs, ...)            -> (codes, scales, group_amax)
+  quantize_colwise(x, ...)                  -> (codes_t, scales_t, amax[, codes, scales])
+  swizzle_scales(scales, rows, cols)        -> scales in the tiled GEMM layout
+  mm(a_codes, a_tiled, a_amax, b_codes, b_tiled, b_amax) -> fp32 a . b^T
 """
 import ctypes
 import os
