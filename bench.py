@@ -331,6 +331,16 @@ def run_fos(args):
     if ws > 1:
         dist.barrier()
     ms = e0.elapsed_time(e1) / args.steps
+    # per-step spread (outside the timed region): each step bracketed by its
+    # own events, inputs still larger than L2
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(min(args.steps, 50))]
+    for a, b in ev:
+        a.record(stream)
+        step()
+        b.record(stream)
+    torch.cuda.synchronize()
+    per_step = sorted(a.elapsed_time(b) for a, b in ev)
     # The dominant kernel, timed in its own loop right after: graphs of the
     # three overlapped stages (fos_quantize_overlap: encode tensor i, amax of
     # tensor i+1); each stage also carries its amax-clear memset, so the
@@ -353,6 +363,10 @@ def run_fos(args):
                        "algorithmic_bytes_per_launch": pipe_bytes,
                        "launch_ms": round(pipe_ms, 5), "peak_kind": peak_kind + " (burst copy)"}
     out["clocks"] = clock_summary
+    if per_step:
+        out["step_ms_spread"] = {"median": round(per_step[len(per_step) // 2], 5),
+                                 "min": round(per_step[0], 5), "max": round(per_step[-1], 5),
+                                 "n": len(per_step)}
 
     if not args.skip_extras:
         out["e2e"] = _e2e(fos, xs, cfg, stream, args, ws, dev)
