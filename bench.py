@@ -556,11 +556,20 @@ def _rows(fos, xs, stream, peak, only=None):
         ws_ = workloads.qdq_weights(8, 2048, 7168, seed=0, device=dev)
         wam = [fos.amax(t) for t in ws_]
         wout = [torch.empty_like(t) for t in ws_]
-        for mode in ("std", "mse_f16", "mae_f16", "mse_f16_seq", "mae_f16_seq"):
-            c = fos.Config(four_over_six=(mode != "std"), mse=not mode.startswith("mae"),
-                           err_f16=True, seq_order=mode.endswith("_seq"))
-            ms = _graph_ms(lambda: fos.qdq(ws_, c, amaxes=wam, outs=wout), 2, stream)
-            rec("qdq_list_8x2048x7168_bf16_" + mode, sum(t.numel() for t in ws_) * 4, ms)
+        def qdq_modes(tag, ts, tam, tout, modes):
+            for mode in modes:
+                c = fos.Config(four_over_six=(mode != "std"), mse=not mode.startswith("mae"),
+                               err_f16="_f16" in mode, seq_order=mode.endswith("_seq"))
+                ms = _graph_ms(lambda: fos.qdq(ts, c, amaxes=tam, outs=tout), 2, stream)
+                rec("qdq_list_8x2048x7168_%s_%s" % (tag, mode), sum(t.numel() for t in ts) * 4, ms)
+        qdq_modes("bf16", ws_, wam, wout, ("std", "mse_f16", "mae_f16", "mse_f16_seq",
+                                           "mae_f16_seq", "mse_exact", "mae_exact"))
+        # the fp16 run of the same list
+        hs_ = workloads.qdq_weights(8, 2048, 7168, seed=0, dtype=torch.float16, device=dev)
+        ham = [fos.amax(t) for t in hs_]
+        hout = [torch.empty_like(t) for t in hs_]
+        qdq_modes("fp16", hs_, ham, hout, ("std", "mse_f16", "mae_f16", "mse_exact", "mae_exact"))
+        del hs_, hout
         # the same list with the per-tensor amax computed: separate amax passes
         # then the QDQ launch, against one fused persistent launch (the bytes
         # counted are the QDQ's, 4 per element, as above: strict)
