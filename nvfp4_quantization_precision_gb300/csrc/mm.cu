@@ -57,26 +57,46 @@ static uint32_t align_of(const void* p) {
     return a;
 }
 
-// One block-scaled GEMM of `mrows` rows of a (codes, tiled scales) against
-// all of b into out[mrows, N].  0: done; 1: no algorithm; 2: a call failed.
-static int lt_gemm(cublasLtHandle_t h, const uint8_t* a_codes, const uint8_t* a_scales,
-                   const uint8_t* b_codes, const uint8_t* b_scales, int64_t mrows, int64_t N,
-                   int64_t K, float* out, cudaStream_t s) {
-    // Column-major view: D (N x mrows, ld N) = op(A') (N x K) * op(B') (K x mrows),
-    // with A' = b's codes as K x N (each column one row of b, K contiguous;
-    // op = T) and B' = a's codes as K x mrows (op = N); D column-major is out
-    // row-major.
+// The cuBLASLt objects of one product, built once per call: the operation
+// (our b as cuBLAS's A, our a as its B) and b's layout, and for each row-chunk
+// height of a the layouts of the a chunk and of the output chunk with the
+// algorithm the heuristic picks for them.  Column-major view of one chunk:
+// D (N x rows, ld N) = op(A') (N x K) * op(B') (K x rows), with A' = b's codes
+// as K x N (each column one row of b, K contiguous; op = T) and B' = the a
+// chunk's codes as K x rows (op = N); D column-major is out row-major.
+struct LtPlan {
+    struct Shape {
+        int64_t rows = -1;
+        cublasLtMatrixLayout_t lb = nullptr, ld = nullptr;
+        cublasLtMatmulAlgo_t algo;
+    };
+    cublasLtHandle_t h = nullptr;
     cublasLtMatmulDesc_t op = nullptr;
-    cublasLtMatrixLayout_t la = nullptr, lb = nullptr, ld = nullptr;
+    cublasLtMatrixLayout_t la = nullptr;
     cublasLtMatmulPreference_t pref = nullptr;
-    int rc = 2;
-    do {
+    Shape sh[2];
+
+    ~LtPlan() {
+        for (Shape& x : sh) {
+            if (x.ld) cublasLtMatrixLayoutDestroy(x.ld);
+            if (x.lb) cublasLtMatrixLayoutDestroy(x.lb);
+        }
+        if (pref) cublasLtMatmulPreferenceDestroy(pref);
+        if (la) cublasLtMatrixLayoutDestroy(la);
+        if (op) cublasLtMatmulDescDestroy(op);
+    }
+
+    // 0: ready; 2: a call failed.  Chunks start on multiples of 256 rows, so
+    // every chunk pointer has the alignment of its base pointer (capped at
+    // 256 bytes, which the heuristic otherwise assumes).
+    int init(const uint8_t* a_codes, const uint8_t* a_scales, const uint8_t* b_codes,
+             const uint8_t* b_scales, const float* out, int64_t N, int64_t K) {
         if (cublasLtMatmulDescCreate(&op, CUBLAS_COMPUTE_32F, CUDA_R_32F) != CUBLAS_STATUS_SUCCESS)
-            break;
+            return 2;
         const cublasOperation_t ta = CUBLAS_OP_T, tb = CUBLAS_OP_N;
         const cublasLtMatmulMatrixScale_t mode = CUBLASLT_MATMUL_MATRIX_SCALE_VEC16_UE4M3;
         const void* sa = b_scales;  // scales of cuBLAS's A (our b)
-        const void* sb = a_scales;  // scales of cuBLAS's B (our a)
+        const void* sb = a_scales;  // scales of cuBLAS's B (our a; moved to each chunk's)
         if (cublasLtMatmulDescSetAttribute(op, CUBLASLT_MATMUL_DESC_TRANSA, &ta, sizeof(ta)) ||
             cublasLtMatmulDescSetAttribute(op, CUBLASLT_MATMUL_DESC_TRANSB, &tb, sizeof(tb)) ||
             cublasLtMatmulDescSetAttribute(op, CUBLASLT_MATMUL_DESC_A_SCALE_MODE, &mode,
@@ -87,14 +107,10 @@ static int lt_gemm(cublasLtHandle_t h, const uint8_t* a_codes, const uint8_t* a_
                                            sizeof(sa)) ||
             cublasLtMatmulDescSetAttribute(op, CUBLASLT_MATMUL_DESC_B_SCALE_POINTER, &sb,
                                            sizeof(sb)))
-            break;
-        if (cublasLtMatrixLayoutCreate(&la, CUDA_R_4F_E2M1, K, N, K) ||
-            cublasLtMatrixLayoutCreate(&lb, CUDA_R_4F_E2M1, K, mrows, K) ||
-            cublasLtMatrixLayoutCreate(&ld, CUDA_R_32F, N, mrows, N))
-            break;
-        if (cublasLtMatmulPreferenceCreate(&pref)) break;
+            return 2;
+        if (cublasLtMatrixLayoutCreate(&la, CUDA_R_4F_E2M1, K, N, K)) return 2;
+        if (cublasLtMatmulPreferenceCreate(&pref)) return 2;
         const size_t ws = 0;
-        // the heuristic assumes 256-byte aligned buffers unless told otherwise
         const uint32_t al_a = align_of(b_codes), al_b = align_of(a_codes), al_d = align_of(out);
         if (cublasLtMatmulPreferenceSetAttribute(pref, CUBLASLT_MATMUL_PREF_MAX_WORKSPACE_BYTES,
                                                  &ws, sizeof(ws)) ||
@@ -106,27 +122,41 @@ static int lt_gemm(cublasLtHandle_t h, const uint8_t* a_codes, const uint8_t* a_
                                                  &al_d, sizeof(al_d)) ||
             cublasLtMatmulPreferenceSetAttribute(pref, CUBLASLT_MATMUL_PREF_MIN_ALIGNMENT_D_BYTES,
                                                  &al_d, sizeof(al_d)))
-            break;
+            return 2;
+        return 0;
+    }
+
+    // Layouts and algorithm for chunks of `rows` rows into slot i.  0: ready;
+    // 1: the library offers no algorithm; 2: a call failed.
+    int shape(int i, int64_t rows, int64_t N, int64_t K) {
+        Shape& x = sh[i];
+        x.rows = rows;
+        if (cublasLtMatrixLayoutCreate(&x.lb, CUDA_R_4F_E2M1, K, rows, K) ||
+            cublasLtMatrixLayoutCreate(&x.ld, CUDA_R_32F, N, rows, N))
+            return 2;
         cublasLtMatmulHeuristicResult_t res = {};
         int found = 0;
-        if (cublasLtMatmulAlgoGetHeuristic(h, op, la, lb, ld, ld, pref, 1, &res, &found) ||
-            found < 1) {
-            rc = 1;
-            break;
-        }
+        if (cublasLtMatmulAlgoGetHeuristic(h, op, la, x.lb, x.ld, x.ld, pref, 1, &res, &found) ||
+            found < 1)
+            return 1;
+        x.algo = res.algo;
+        return 0;
+    }
+
+    // One chunk: its a codes and tiled scales against all of b.
+    int run(const Shape& x, const uint8_t* a_codes, const uint8_t* a_scales,
+            const uint8_t* b_codes, float* out, cudaStream_t s) {
+        const void* sb = a_scales;  // scales of cuBLAS's B (our a chunk)
+        if (cublasLtMatmulDescSetAttribute(op, CUBLASLT_MATMUL_DESC_B_SCALE_POINTER, &sb,
+                                           sizeof(sb)))
+            return 2;
         const float alpha = 1.0f, beta = 0.0f;
-        if (cublasLtMatmul(h, op, &alpha, b_codes, la, a_codes, lb, &beta, out, ld, out, ld,
-                           &res.algo, nullptr, 0, s))
-            break;
-        rc = 0;
-    } while (false);
-    if (pref) cublasLtMatmulPreferenceDestroy(pref);
-    if (ld) cublasLtMatrixLayoutDestroy(ld);
-    if (lb) cublasLtMatrixLayoutDestroy(lb);
-    if (la) cublasLtMatrixLayoutDestroy(la);
-    if (op) cublasLtMatmulDescDestroy(op);
-    return rc;
-}
+        if (cublasLtMatmul(h, op, &alpha, b_codes, la, a_codes, x.lb, &beta, out, x.ld, out, x.ld,
+                           &x.algo, nullptr, 0, s))
+            return 2;
+        return 0;
+    }
+};
 
 // Rows of a per GEMM: a multiple of 256 whose fp32 output slice takes about
 // half of the L2, so that the epilogue that follows each GEMM reads D back
@@ -147,15 +177,21 @@ static int64_t chunk_rows(int64_t M, int64_t N, int dev) {
 int run_mm(const uint8_t* a_codes, const uint8_t* a_scales, const float* a_amax, int a_row,
            const uint8_t* b_codes, const uint8_t* b_scales, const float* b_amax, int64_t M,
            int64_t N, int64_t K, float six_bound, float* out, int dev, cudaStream_t s) {
-    cublasLtHandle_t h = lt_handle(dev);
-    if (!h) return 2;
+    LtPlan plan;
+    plan.h = lt_handle(dev);
+    if (!plan.h) return 2;
+    int rc = plan.init(a_codes, a_scales, b_codes, b_scales, out, N, K);
+    if (rc) return rc;
     const int64_t mc = chunk_rows(M, N, dev);
+    const int64_t tail = M % mc;
+    if ((rc = plan.shape(0, mc, N, K))) return rc;
+    if (tail && (rc = plan.shape(1, tail, N, K))) return rc;
     // a's tiled scales: 128-row tile rows of 128 * (K / 16) bytes (K % 64 == 0),
     // so a chunk that starts on a multiple of 128 rows starts at m0 * K / 16.
     for (int64_t m0 = 0; m0 < M; m0 += mc) {
         const int64_t rows = (M - m0 < mc) ? (M - m0) : mc;
-        const int rc = lt_gemm(h, a_codes + m0 * (K / 2), a_scales + m0 * (K / 16), b_codes,
-                               b_scales, rows, N, K, out + m0 * N, s);
+        rc = plan.run(rows == mc ? plan.sh[0] : plan.sh[1], a_codes + m0 * (K / 2),
+                      a_scales + m0 * (K / 16), b_codes, out + m0 * N, s);
         if (rc) return rc;
         int64_t blocks = rows;
         const int64_t cap = (int64_t)sm_count() * 8;
