@@ -280,9 +280,9 @@ FOS_API fos_status fos_qdq(int n, const void* const* x, void* const* out, const 
  * persistent launch (the only other work on the stream is a clear of the
  * workspace): the launch runs the amax pass of tensor 0, then
  * quantize-dequantizes tensor i while it computes the amax of tensor i+1
- * (the survey's "fused multi-tensor amax + QDQ in one persistent launch";
- * the Megatron PR computes each weight's amax with a separate PyTorch
- * reduction first).  Knobs, layouts and results are those of fos_qdq with
+ * (the Megatron PR, "Fused data path", computes each weight's amax with a
+ * separate PyTorch reduction first and lists the per-weight launches among
+ * its pending work).  Knobs, layouts and results are those of fos_qdq with
  * cfg->amax_is_input = 0, which this call requires; amax[i] receives tensor
  * i's amax.  n <= FOS_QDQ_MAX_LIST.
  *   workspace: the warps of the launch wait for one another (a tensor's QDQ
