@@ -43,6 +43,7 @@
 #ifndef FOS_H
 #define FOS_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #if defined(__GNUC__)

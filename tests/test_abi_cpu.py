@@ -260,3 +260,39 @@ def test_check_tile_amax_rejects_before_any_cuda_call(L):
     assert L.fos_check_tile_amax(FAKE, i64(16), ctypes.c_void_p(0x10004),
                                  None) == fos.FOS_ERR_MISALIGNED
     assert L.fos_tile_amax_status(None, None) == fos.FOS_ERR_INVALID_ARG
+
+
+C_PROGRAM = r"""
+#include <stdio.h>
+#include <string.h>
+#include "fos.h"
+#include "fos_diag.h"
+int main(void) {
+    fos_config cfg;
+    memset(&cfg, 0, sizeof cfg);
+    cfg.e4m3_bound = 448;
+    /* host validation only: a 24-column tensor is rejected before any CUDA call */
+    fos_status st = fos_quantize((const void*)0x10000, FOS_BF16, 32, 24, &cfg, 0, 0, 0, 0);
+    printf("%d %d %s\n", fos_version(), (int)st, fos_status_string(st));
+    return st == FOS_ERR_UNSUPPORTED ? 0 : 1;
+}
+"""
+
+
+@pytest.mark.parametrize("lang", ["c", "c++"])
+def test_headers_compile_and_link_from_plain_c(L, tmp_path, lang):
+    """The public headers stand alone in C99 and C++17, and a plain C program
+    links against the library and calls it (host-side calls only)."""
+    import subprocess
+    src = tmp_path / ("prog.c" if lang == "c" else "prog.cpp")
+    src.write_text(C_PROGRAM)
+    exe = tmp_path / "prog"
+    cc = ["gcc", "-std=c99"] if lang == "c" else ["g++", "-std=c++17"]
+    libdir = os.path.dirname(fos.LIB_PATH)
+    r = subprocess.run(cc + ["-Wall", "-Wextra", "-Werror", "-I", os.path.join(ROOT, "include"),
+                             str(src), "-o", str(exe), "-L", libdir, "-lfos",
+                             "-Wl,-rpath," + libdir], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    out = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert out.returncode == 0, out.stdout + out.stderr
+    assert out.stdout.split()[0] == "10000"
