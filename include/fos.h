@@ -216,6 +216,10 @@ FOS_API fos_status fos_quantize_colwise(const void* x, fos_dtype dt, int64_t row
  * out holds fos_swizzled_scales_bytes(rows, cols) bytes (4-byte aligned).
  * The pages pass plain scales to their GEMMs; this is the layout a GEMM
  * library's NVFP4 path takes, checked in the tests against such a GEMM.
+ * fos_swizzled_scales_bytes returns -1 for negative sizes or cols % 16 != 0.
+ * Errors: FOS_ERR_INVALID_ARG (negative sizes, null or non-device pointers
+ * with a nonzero size), FOS_ERR_UNSUPPORTED (cols % 16 != 0),
+ * FOS_ERR_MISALIGNED (out not 4-byte aligned).
  */
 FOS_API int64_t fos_swizzled_scales_bytes(int64_t rows, int64_t cols);
 FOS_API fos_status fos_swizzle_scales(const uint8_t* scales, int64_t rows, int64_t cols,
@@ -268,8 +272,13 @@ FOS_API fos_status fos_dequantize(const uint8_t* codes, const uint8_t* scales, c
  *   the per-tensor amax: read when cfg->amax_is_input, else computed and
  *   written first.  Only 1x16 blocks and FOS_SCALE_TENSOR (the pages'
  *   non-goals exclude 2D blocks and row scaling for this path).
- * The host arrays x, out, rows, cols, amax must hold n entries each.
+ * The host arrays x, out, rows, cols, amax must hold n entries each; the
+ * data pointers of an empty tensor (rows or cols 0) may be null.
  * Result equals fos_dequantize(fos_quantize(x)) bit for bit.
+ * Errors: FOS_ERR_INVALID_ARG (n < 0, null arrays or pointers, bad enum,
+ * tensors on different devices), FOS_ERR_UNSUPPORTED (fp32, 16x16 blocks,
+ * per-row scale, cols % 16 != 0), FOS_ERR_MISALIGNED (x or out not 32-byte
+ * aligned).
  */
 #define FOS_QDQ_MAX_LIST 64
 FOS_API fos_status fos_qdq(int n, const void* const* x, void* const* out, const int64_t* rows,
@@ -352,6 +361,11 @@ FOS_API fos_status fos_workspace_error(const void* workspace, fos_stream_t strea
  *   computed (NaN-dropping, empty group -> 0) and written.
  *   cfg->granularity is ignored (the group amax is the global scale source).
  *   1 <= G <= FOS_GROUPED_MAX_GROUPS.
+ * Errors: FOS_ERR_INVALID_ARG (G < 1, null pointers, bad enum, pointers on
+ * different devices), FOS_ERR_UNSUPPORTED (G above the maximum, cols % 16,
+ * 16x16 with rows % 16, a bad bound, the sequential order with 16x16),
+ * FOS_ERR_MISALIGNED (x not 32-byte, codes not 8-byte, offs not 4-byte
+ * aligned).
  */
 #define FOS_GROUPED_MAX_GROUPS 8192
 FOS_API fos_status fos_quantize_grouped(const void* x, fos_dtype dt, int64_t rows, int64_t cols,

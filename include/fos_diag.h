@@ -39,6 +39,10 @@ enum {
     FOS_DIAG_DIV6 = 7
 };
 
+/* fos_diag_convert -- applies `op` to n elements of the device buffer `in`
+ * and writes `out` (device, caller-owned).  Pairwise ops leave the last
+ * output element unwritten when n is odd.  Errors: FOS_ERR_INVALID_ARG (bad
+ * op, n < 0, null or non-device pointers, buffers on different devices). */
 FOS_API fos_status fos_diag_convert(int op, const void* in, void* out, int64_t n, fos_stream_t stream);
 
 /*
