@@ -296,3 +296,57 @@ def test_headers_compile_and_link_from_plain_c(L, tmp_path, lang):
     out = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
     assert out.returncode == 0, out.stdout + out.stderr
     assert out.stdout.split()[0] == "10000"
+
+
+def test_swizzled_scales_bytes_matches_the_oracle_layout(L):
+    """The host-side size of the tiled scale layout equals the size of the
+    oracle's layout for the same scale matrix; bad shapes give -1."""
+    import numpy as np
+
+    import oracle
+    L.fos_swizzled_scales_bytes.argtypes = [ctypes.c_int64, ctypes.c_int64]
+    L.fos_swizzled_scales_bytes.restype = ctypes.c_int64
+    for rows, cols in [(1, 16), (127, 48), (128, 64), (129, 80), (300, 144), (8192, 4096)]:
+        want = oracle.swizzle_scales(np.zeros((rows, cols // 16), np.uint8)).size
+        assert L.fos_swizzled_scales_bytes(rows, cols) == want, (rows, cols)
+    assert L.fos_swizzled_scales_bytes(0, 64) == 0
+    for rows, cols in [(-1, 16), (16, -16), (16, 24)]:
+        assert L.fos_swizzled_scales_bytes(rows, cols) == -1
+
+
+def test_host_validation_fuzz_never_crashes(L):
+    """Seeded random argument sets (negative, zero, ragged and huge sizes,
+    invalid enums, null, fake and misaligned pointers) for every data entry
+    point: each call returns a defined status and nothing crashes.  No GPU is
+    present, so a call that passes validation stops at the pointer check."""
+    import random
+    rng = random.Random(12345)
+    i64 = ctypes.c_int64
+    sizes = [-16, -1, 0, 1, 15, 16, 17, 32, 48, 4096, 1 << 40, (1 << 62)]
+    ptrs = [None, FAKE, ctypes.c_void_p(0x10001), ctypes.c_void_p(0x10010)]
+    for n in ("fos_quantize", "fos_dequantize", "fos_quantize_grouped", "fos_quantize_colwise",
+              "fos_swizzle_scales", "fos_check_tile_amax", "fos_mm", "fos_amax"):
+        getattr(L, n).restype = ctypes.c_int
+    valid = set(range(6))
+    for _ in range(400):
+        cfg = _cfg(block=rng.choice([0, 1, 2]), mode=rng.choice([0, 1, 3]),
+                   err_metric=rng.choice([0, 1, -1]), err_precision=rng.choice([0, 1, 2]),
+                   e4m3_bound=rng.choice([448, 256, 100]), granularity=rng.choice([0, 1, 5]),
+                   amax_is_input=rng.choice([0, 1, 2]), err_order=rng.choice([0, 1, 9]))
+        R, C = i64(rng.choice(sizes)), i64(rng.choice(sizes))
+        p = [rng.choice(ptrs) for _ in range(6)]
+        dt = rng.choice([0, 1, 2, 7])
+        rcs = [
+            L.fos_quantize(p[0], dt, R, C, ctypes.byref(cfg), p[1], p[2], p[3], None),
+            L.fos_dequantize(p[0], p[1], p[2], R, C, ctypes.byref(cfg), p[3], dt, None),
+            L.fos_quantize_grouped(p[0], dt, R, C, p[1], rng.choice([-1, 0, 1, 64, 9000]),
+                                   ctypes.byref(cfg), p[2], p[3], p[4], None),
+            L.fos_quantize_colwise(p[0], dt, R, C, ctypes.byref(cfg), p[1], p[2], p[3], p[4],
+                                   p[5], None),
+            L.fos_swizzle_scales(p[0], R, C, p[1], None),
+            L.fos_check_tile_amax(p[0], R, p[1], None),
+            L.fos_mm(p[0], p[1], p[2], p[3], p[4], p[5], R, C, i64(rng.choice(sizes)),
+                     ctypes.byref(cfg), p[0], None),
+            L.fos_amax(p[0], dt, R, C, rng.choice([0, 1, 4]), p[1], None),
+        ]
+        assert all(rc in valid for rc in rcs), rcs
