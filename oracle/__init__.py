@@ -246,6 +246,41 @@ def swizzle_scales(scales):
     return out
 
 
+def block_values(codes, scales):
+    """The value v * sigma of every element of 1x16 codes [R, C/2] and E4M3
+    block scales [R, C/16] (the standard NVFP4 decode without the global
+    scale), exact in binary64: an E2M1 value times an E4M3 value has at most
+    seven significant bits."""
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    R, C2 = codes.shape
+    q = np.empty((R, 2 * C2), np.uint32)
+    q[:, 0::2], q[:, 1::2] = codes & 0xF, codes >> 4
+    v = np.vectorize(e2m1_value, otypes=[np.float64])(q)
+    sig = np.vectorize(e4m3_value, otypes=[np.float64])(np.asarray(scales, np.uint32))
+    return v * np.repeat(sig, 16, axis=1)
+
+
+def mm_reference(a_codes, a_scales, a_amax, b_codes, b_scales, b_amax, cfg: Config):
+    """The product of quantized operands, out = a . b^T (grouped PR, the
+    four_over_six_mm forward), as the binary64 product of the block values
+    (its rounding far below the bound) times the FP32 global decode scales
+    g = rn(1 / S) (S from the amax
+    as quantization computed it; per row of a when cfg.row_scaled), together
+    with the bound any FP32 evaluation must meet: K products summed in any
+    order plus the two epilogue multiplies, gamma_(K+2) * sum |terms| * |g_a g_b|
+    with gamma_n = n u / (1 - n u), u = 2^-24.  Returns (ref, bound)."""
+    pa, pb = block_values(a_codes, a_scales), block_values(b_codes, b_scales)
+    K = pa.shape[1]
+    ga = np.float32(1.0) / np.array([global_scale(float(v), cfg.bound)
+                                     for v in np.ravel(a_amax)], np.float32)
+    gb = np.float32(1.0) / np.float32(global_scale(float(np.ravel(b_amax)[0]), cfg.bound))
+    ga = ga.astype(np.float64).reshape(-1, 1) if cfg.row_scaled else np.float64(ga[0])
+    g = ga * np.float64(gb)
+    n = K + 2
+    gamma = n * 2.0 ** -24 / (1.0 - n * 2.0 ** -24)
+    return (pa @ pb.T) * g, gamma * (np.abs(pa) @ np.abs(pb).T) * np.abs(g)
+
+
 def count_nonuniform_tiles(amax):
     """The tile-uniform contract of 16x16 blocks with a row-scaled global
     scale (grouped PR: the 16 rows of a tile share one amax): the number of

@@ -817,24 +817,12 @@ def test_swizzled_scales_feed_an_fp4_gemm(mode):
 
 
 # ------------------------------------------------------------------ product of quantized operands
-def _block_values(codes, scales):
-    """v * sigma per element (exact in binary64) from 1x16 codes and scales."""
-    R, C2 = codes.shape
-    lo = (codes & 0xF).astype(np.uint32)
-    hi = (codes >> 4).astype(np.uint32)
-    q = np.empty((R, 2 * C2), np.uint32)
-    q[:, 0::2], q[:, 1::2] = lo, hi
-    v = np.vectorize(oracle.e2m1_value, otypes=[np.float64])(q)
-    sig = np.vectorize(oracle.e4m3_value, otypes=[np.float64])(scales.astype(np.uint32))
-    return v * np.repeat(sig, 16, axis=1)
-
-
 @pytest.mark.parametrize("mode", ["std", "mse"])
 @pytest.mark.parametrize("row", [False, True])
 def test_mm_of_quantized_operands(mode, row):
-    """a . b^T from this library's codes and tiled scales equals the product
-    of the oracle's block values of the same inputs, divided by the global
-    scales, within the fp32 accumulation bound (K + 2) * 2^-24 * sum |terms|."""
+    """a . b^T from this library's codes and tiled scales equals the oracle's
+    product reference (block values of the same inputs times the global
+    decode scales) within its fp32 bound gamma_(K+2) * sum |terms|."""
     M, N, K = 256, 128, 512
     gcfg_a, ocfg_a = _cfgs(mode, 448, row)
     gcfg_b, ocfg_b = _cfgs(mode, 448)
@@ -848,15 +836,9 @@ def test_mm_of_quantized_operands(mode, row):
     oca, osa, oaa = oracle.quantize(a.float().numpy(), ocfg_a)
     ocb, osb, oab = oracle.quantize(b.float().numpy(), ocfg_b)
     assert np.array_equal(ca.cpu().numpy(), oca) and np.array_equal(cb.cpu().numpy(), ocb)
-    pa, pb = _block_values(oca, osa), _block_values(ocb, osb)
-    D = pa @ pb.T
-    bound = (K + 2) * 2.0 ** -24 * (np.abs(pa) @ np.abs(pb).T)
-    ga = 1.0 / np.array([oracle.global_scale(float(v), 448) for v in oaa], np.float32)
-    gb = 1.0 / np.float32(oracle.global_scale(float(oab[0]), 448))
-    ga = ga.reshape(-1, 1) if row else ga.reshape(1, 1)
-    ref = D * ga * gb
+    ref, bound = oracle.mm_reference(oca, osa, oaa, ocb, osb, oab, ocfg_a)
     err = np.abs(out.cpu().numpy().astype(np.float64) - ref)
-    assert np.all(err <= bound * np.abs(ga * gb) + 1e-30), float((err / (bound * np.abs(ga * gb) + 1e-30)).max())
+    assert np.all(err <= bound + 1e-30), float((err / (bound + 1e-30)).max())
 
 
 def _at16(t):
@@ -891,11 +873,6 @@ def test_mm_in_row_chunks_with_16_byte_aligned_operands():
     ocb, osb, oab = oracle.quantize(b.float().numpy(), ocfg_b)
     assert np.array_equal(ca.cpu().numpy(), oca) and np.array_equal(cb.cpu().numpy(), ocb)
     rows = np.unique(np.concatenate([np.arange(0, M, 97), [M - 1, M - 16, 767, 768, 1536]]))
-    pa, pb = _block_values(oca[rows], osa[rows]), _block_values(ocb, osb)
-    ga = (1.0 / np.array([oracle.global_scale(float(v), 448) for v in oaa[rows]],
-                         np.float32)).reshape(-1, 1)
-    gb = 1.0 / np.float32(oracle.global_scale(float(oab[0]), 448))
-    ref = (pa @ pb.T) * ga * gb
-    bound = (K + 2) * 2.0 ** -24 * (np.abs(pa) @ np.abs(pb).T) * np.abs(ga * gb)
+    ref, bound = oracle.mm_reference(oca[rows], osa[rows], oaa[rows], ocb, osb, oab, ocfg_a)
     err = np.abs(got.cpu().numpy()[rows].astype(np.float64) - ref)
     assert np.all(err <= bound + 1e-30), float((err / (bound + 1e-30)).max())

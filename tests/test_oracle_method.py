@@ -586,3 +586,38 @@ def test_tile_uniform_count_hand_cases(orc):
     assert orc.count_nonuniform_tiles(np.zeros(0, np.float32)) == 0
     with pytest.raises(ValueError):
         orc.count_nonuniform_tiles(np.ones(17, np.float32))
+
+
+@pytest.mark.parametrize("row", [False, True])
+def test_mm_reference_hand_operands(orc, row):
+    """The product reference on operands written by hand: a[0,0] = 1.0 and
+    a[1,17] = 6 under a block scale of 2 (code 0x40); b[0,0] = 1.5 and
+    b[1,17] = -1.0; every other element 0, every other scale 1.0 (0x38).
+    amax 2688 gives S = 1 (g = 1); with a row scale, row 1 of a has amax
+    1344, S = 2, g = 0.5.  Expected out[0,0] = 1.5 and out[1,1] = -12
+    (-6 row-scaled), zeros elsewhere; the bound is gamma_(K+2) times the
+    absolute sum of the terms."""
+    M = N = 16
+    K = 64
+    ac = np.zeros((M, K // 2), np.uint8)
+    bc = np.zeros((N, K // 2), np.uint8)
+    as_ = np.full((M, K // 16), 0x38, np.uint8)
+    bs = np.full((N, K // 16), 0x38, np.uint8)
+    ac[0, 0] = 0x02          # element 0 (low nibble): 1.0
+    ac[1, 8] = 0x70          # element 17 (high nibble of byte 8): 6
+    as_[1, 1] = 0x40         # block 1 of row 1: scale 2.0
+    bc[0, 0] = 0x03          # 1.5
+    bc[1, 8] = 0xA0          # element 17: -1.0
+    a_amax = np.full(M if row else 1, 2688.0, np.float32)
+    if row:
+        a_amax[1] = 1344.0
+    cfg = orc.Config(row_scaled=row)
+    ref, bound = orc.mm_reference(ac, as_, a_amax, bc, bs, np.array([2688.0], np.float32), cfg)
+    want = np.zeros((M, N))
+    want[0, 0] = 1.5
+    want[1, 1] = -6.0 if row else -12.0
+    assert np.array_equal(ref, want)
+    n = K + 2
+    gamma = n * 2.0 ** -24 / (1 - n * 2.0 ** -24)
+    assert bound[0, 0] == gamma * 1.5 and bound[1, 1] == gamma * abs(want[1, 1])
+    assert np.count_nonzero(bound) == 2
