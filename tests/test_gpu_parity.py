@@ -716,10 +716,12 @@ def test_quantize_colwise_full_size_sampled():
     c1, s1, a1 = fos.quantize(x, gcfg)
     torch.cuda.synchronize()
     assert torch.equal(a, a1) and torch.equal(c, c1) and torch.equal(s_, s1)
+    oa = oracle.amax_tensor(x.cpu().float().numpy())  # the whole tensor, on the host
+    assert np.array_equal(_u32(a), oa.view(np.uint32))
     cols = np.random.default_rng(4).choice(4096, 24, replace=False)
     xc = x[:, torch.from_numpy(cols).to(DEV)].cpu().float().numpy()  # [8192, 24]
     ocfg2 = oracle.Config(**{**ocfg.__dict__, "amax_is_input": True})
-    oct_, ost, _ = oracle.quantize_colwise(xc, ocfg2, amax=a.cpu().numpy())
+    oct_, ost, _ = oracle.quantize_colwise(xc, ocfg2, amax=oa)
     assert np.array_equal(ct.cpu().numpy()[cols], oct_)
     assert np.array_equal(st.cpu().numpy()[cols], ost)
 
