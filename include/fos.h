@@ -323,9 +323,13 @@ FOS_API fos_status fos_qdq_fused(int n, const void* const* x, void* const* out,
  * GPU that loads it, kept until the process exits), so lists are limited to
  * n <= FOS_QDQ_MAX_LIST (64); longer lists return FOS_ERR_UNSUPPORTED.
  * Nothing is allocated: no cudaMalloc, no cudaFree, no allocating library
- * call.  The first call on a device looks up the array's device address
- * (with that device current) and caches it; make that first call before any
- * stream capture.  Each call clears the array on `stream` before its launch.
+ * call.  Each call looks up the array's device address on the data's device
+ * (with that device current), so a reset of that device's primary context
+ * between calls is harmless; while `stream` is being captured the address
+ * of the previous lookup is reused instead, so make the first call on a
+ * device before any stream capture.  Host-side argument checks are those of
+ * fos_qdq_fused, in the same order, and come before any CUDA call.  Each
+ * call clears the array on `stream` before its launch.
  * Every call on a device shares the one array: calls whose work may overlap
  * on the GPU (other streams, other threads) race and give wrong results;
  * order them on one stream.  A wait that runs out is recorded in the array

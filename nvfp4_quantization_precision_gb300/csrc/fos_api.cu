@@ -660,6 +660,38 @@ fos_status fos_diag_wait_timeout(int which, uint32_t* word, fos_stream_t stream)
 }  // extern "C"
 
 // ------------------------------------------------------------ fused amax + QDQ
+namespace fos {
+
+// Host-only checks of a fused amax + QDQ list call, in the order both fused
+// entry points report them: list length sign, dtype, configuration, the
+// supported knobs, list length limit, then pointers, shapes and alignment of
+// every tensor.  Makes no CUDA call.
+fos_status qdq_fused_host_checks(int n, int max_n, const void* const* x, void* const* out,
+                                 const int64_t* rows, const int64_t* cols, float* const* amax,
+                                 fos_dtype dt, const fos_config* cfg) {
+    if (n < 0) return FOS_ERR_INVALID_ARG;
+    if (dt != FOS_BF16 && dt != FOS_FP16) return valid_dtype(dt) ? FOS_ERR_UNSUPPORTED
+                                                                  : FOS_ERR_INVALID_ARG;
+    fos_status st = check_config(cfg);
+    if (st) return st;
+    if (cfg->block != FOS_BLOCK_1X16 || cfg->granularity != FOS_SCALE_TENSOR ||
+        cfg->amax_is_input)
+        return FOS_ERR_UNSUPPORTED;
+    if (n > max_n) return FOS_ERR_UNSUPPORTED;
+    if (n == 0) return FOS_OK;
+    if (!x || !out || !rows || !cols || !amax) return FOS_ERR_INVALID_ARG;
+    for (int i = 0; i < n; ++i) {
+        st = check_shape(rows[i], cols[i], false);
+        if (st) return st;
+        const bool empty = rows[i] == 0 || cols[i] == 0;
+        if (!amax[i] || (!empty && (!x[i] || !out[i]))) return FOS_ERR_INVALID_ARG;
+        if (!empty && (!aligned(x[i], 32) || !aligned(out[i], 32))) return FOS_ERR_MISALIGNED;
+    }
+    return FOS_OK;
+}
+
+}  // namespace fos
+
 extern "C" {
 
 size_t fos_qdq_fused_workspace_bytes(int n) {
@@ -672,27 +704,12 @@ fos_status fos_qdq_fused(int n, const void* const* x, void* const* out, const in
                          const int64_t* cols, float* const* amax, fos_dtype dt,
                          const fos_config* cfg, void* workspace, size_t workspace_bytes,
                          fos_stream_t stream) {
-    if (n < 0) return FOS_ERR_INVALID_ARG;
-    if (dt != FOS_BF16 && dt != FOS_FP16) return valid_dtype(dt) ? FOS_ERR_UNSUPPORTED
-                                                                  : FOS_ERR_INVALID_ARG;
-    fos_status st = check_config(cfg);
-    if (st) return st;
-    if (cfg->block != FOS_BLOCK_1X16 || cfg->granularity != FOS_SCALE_TENSOR ||
-        cfg->amax_is_input)
-        return FOS_ERR_UNSUPPORTED;
-    if (n > kQdqMaxList) return FOS_ERR_UNSUPPORTED;
-    if (n == 0) return FOS_OK;
-    if (!x || !out || !rows || !cols || !amax || !workspace) return FOS_ERR_INVALID_ARG;
+    fos_status st = qdq_fused_host_checks(n, kQdqMaxList, x, out, rows, cols, amax, dt, cfg);
+    if (st || n == 0) return st;
+    if (!workspace) return FOS_ERR_INVALID_ARG;
     const size_t need = fos_qdq_fused_workspace_bytes(n);
     if (workspace_bytes < need) return FOS_ERR_INVALID_ARG;
     if (!aligned(workspace, 256)) return FOS_ERR_MISALIGNED;
-    for (int i = 0; i < n; ++i) {
-        st = check_shape(rows[i], cols[i], false);
-        if (st) return st;
-        const bool empty = rows[i] == 0 || cols[i] == 0;
-        if (!amax[i] || (!empty && (!x[i] || !out[i]))) return FOS_ERR_INVALID_ARG;
-        if (!empty && (!aligned(x[i], 32) || !aligned(out[i], 32))) return FOS_ERR_MISALIGNED;
-    }
     int dev = device_of(workspace);
     if (dev < 0) return FOS_ERR_INVALID_ARG;
     for (int i = 0; i < n; ++i) {

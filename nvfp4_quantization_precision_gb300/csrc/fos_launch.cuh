@@ -7,6 +7,7 @@
 #include <mutex>
 #include <unordered_map>
 
+#include "fos.h"
 #include "fos_kernels.cuh"
 
 namespace fos {
@@ -130,5 +131,11 @@ int run_mm(const uint8_t* a_codes, const uint8_t* a_scales, const float* a_amax,
 cudaError_t launch_swizzle(const uint8_t* scales, int64_t rows, int64_t nb, uint8_t* out,
                            cudaStream_t);
 cudaError_t launch_check_tile_amax(const float* amax, int64_t rows, int64_t* bad, cudaStream_t);
+
+// Host-side argument checks shared by the two fused amax + QDQ entry points
+// (fos_api.cu); no CUDA call.
+fos_status qdq_fused_host_checks(int n, int max_n, const void* const* x, void* const* out,
+                                 const int64_t* rows, const int64_t* cols, float* const* amax,
+                                 fos_dtype dt, const fos_config* cfg);
 
 }  // namespace fos

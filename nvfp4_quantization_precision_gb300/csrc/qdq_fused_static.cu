@@ -23,7 +23,7 @@ static __device__ __align__(256) uint32_t g_qdq_fused_ws[kStaticWords];
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
-void* g_addr[kMaxDevices] = {};  // device address of g_qdq_fused_ws, per device
+void* g_addr[kMaxDevices] = {};  // last looked-up device address of g_qdq_fused_ws, per device
 
 // Device of the first non-empty tensor (or of amax[0] when all are empty).
 int list_device(int n, const void* const* x, const int64_t* rows, const int64_t* cols,
@@ -43,12 +43,27 @@ int list_device(int n, const void* const* x, const int64_t* rows, const int64_t*
     return at.device;
 }
 
-// The array's device address on `dev`, looked up once per device with that
-// device current (the caller's current device is restored).
-void* workspace_on(int dev) {
+// True when `s` is being captured into a graph (or its state cannot be read).
+bool capturing(cudaStream_t s) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) {
+        cudaGetLastError();
+        return true;
+    }
+    return cs != cudaStreamCaptureStatusNone;
+}
+
+// The array's device address on `dev`, looked up with that device current
+// (the caller's current device is restored).  Outside stream capture the
+// address is looked up again on every call, so a reset of the device's
+// primary context between calls (which reloads the module and moves the
+// array) is picked up; during capture the address of the last lookup on
+// that device is used, so a device's first call must come before any
+// capture.
+void* workspace_on(int dev, cudaStream_t s) {
     if (dev < 0 || dev >= kMaxDevices) return nullptr;
     std::lock_guard<std::mutex> g(g_mu);
-    if (g_addr[dev]) return g_addr[dev];
+    if (g_addr[dev] && capturing(s)) return g_addr[dev];
     int prev = -1;
     if (cudaGetDevice(&prev) != cudaSuccess) {
         cudaGetLastError();
@@ -65,7 +80,7 @@ void* workspace_on(int dev) {
         ptr = nullptr;
     }
     if (prev != dev) cudaSetDevice(prev);
-    if (ptr) g_addr[dev] = ptr;
+    g_addr[dev] = ptr;
     return ptr;
 }
 
@@ -76,16 +91,17 @@ extern "C" {
 fos_status fos_qdq_fused_static(int n, const void* const* x, void* const* out,
                                 const int64_t* rows, const int64_t* cols, float* const* amax,
                                 fos_dtype dt, const fos_config* cfg, fos_stream_t stream) {
-    if (n < 0) return FOS_ERR_INVALID_ARG;
-    if (n > kStaticMaxList) return FOS_ERR_UNSUPPORTED;  // beyond the fixed workspace
-    if (n == 0) return FOS_OK;
-    if (!x || !out || !rows || !cols || !amax || !amax[0]) return FOS_ERR_INVALID_ARG;
+    // the same host-only checks, in the same order, as fos_qdq_fused, with
+    // the fixed array's list limit; no CUDA call before they pass
+    const fos_status st =
+        fos::qdq_fused_host_checks(n, kStaticMaxList, x, out, rows, cols, amax, dt, cfg);
+    if (st || n == 0) return st;
     const int dev = list_device(n, x, rows, cols, amax);
     if (dev < 0) return FOS_ERR_INVALID_ARG;
-    void* ws = workspace_on(dev);
+    void* ws = workspace_on(dev, reinterpret_cast<cudaStream_t>(stream));
     if (!ws) return FOS_ERR_CUDA;
-    // fos_qdq_fused validates everything else and clears the words it uses
-    // (with cudaMemsetAsync on `stream`) before its launch.
+    // fos_qdq_fused checks the devices of every pointer and clears the words
+    // it uses (with cudaMemsetAsync on `stream`) before its launch.
     return fos_qdq_fused(n, x, out, rows, cols, amax, dt, cfg, ws,
                          kStaticWords * sizeof(uint32_t), stream);
 }

@@ -205,6 +205,48 @@ def test_qdq_fused_rejects_before_any_cuda_call(L):
     assert call(n=0) == fos.FOS_OK
 
 
+def test_qdq_fused_static_rejects_like_the_workspace_form_before_any_cuda_call(L):
+    """fos_qdq_fused_static runs the host checks of fos_qdq_fused in the same
+    order (dtype and configuration before the list length), before it
+    resolves a device or its fixed array."""
+    P1 = ctypes.c_void_p * 1
+    x, o, a = P1(FAKE), P1(FAKE), P1(FAKE)
+    rows, cols = (ctypes.c_int64 * 1)(16), (ctypes.c_int64 * 1)(16)
+
+    def call(n=1, cfg=None, dt=0, amax=a, nullcfg=False):
+        c = cfg or _cfg(amax_is_input=0)
+        return L.fos_qdq_fused_static(n, x, o, rows, cols, amax, dt,
+                                      None if nullcfg else ctypes.byref(c), None)
+    assert call(cfg=_cfg(amax_is_input=1)) == fos.FOS_ERR_UNSUPPORTED
+    assert call(cfg=_cfg(amax_is_input=0, block=1)) == fos.FOS_ERR_UNSUPPORTED
+    assert call(cfg=_cfg(amax_is_input=0, granularity=1)) == fos.FOS_ERR_UNSUPPORTED
+    assert call(dt=2) == fos.FOS_ERR_UNSUPPORTED
+    assert call(n=65) == fos.FOS_ERR_UNSUPPORTED
+    assert call(n=-1) == fos.FOS_ERR_INVALID_ARG
+    # bad dtype / config win over the list length, like fos_qdq_fused
+    assert call(n=0, dt=7) == fos.FOS_ERR_INVALID_ARG
+    assert call(n=0, nullcfg=True) == fos.FOS_ERR_INVALID_ARG
+    assert call(n=65, dt=7) == fos.FOS_ERR_INVALID_ARG
+    assert call(n=0, cfg=_cfg(amax_is_input=0, e4m3_bound=100)) == fos.FOS_ERR_UNSUPPORTED
+    assert call(amax=P1(None)) == fos.FOS_ERR_INVALID_ARG
+    c2 = (ctypes.c_int64 * 1)(24)
+    assert L.fos_qdq_fused_static(1, x, o, rows, c2, a, 0, ctypes.byref(_cfg(amax_is_input=0)),
+                                  None) == fos.FOS_ERR_UNSUPPORTED
+    mis = P1(ctypes.c_void_p(0x10010))
+    assert L.fos_qdq_fused_static(1, mis, o, rows, cols, a, 0,
+                                  ctypes.byref(_cfg(amax_is_input=0)), None) == \
+        fos.FOS_ERR_MISALIGNED
+    assert call(n=0) == fos.FOS_OK
+    for n in (0, 1, 65):
+        for dt in (0, 1, 2, 7):
+            want = L.fos_qdq_fused(n, x, o, rows, cols, a, dt,
+                                   ctypes.byref(_cfg(amax_is_input=0)),
+                                   ctypes.c_void_p(0x100000), 1 << 20, None)
+            got = call(n=n, dt=dt)
+            if want != fos.FOS_OK or n == 0:
+                assert got == want, (n, dt, got, want)
+
+
 def test_workspace_error_rejects_null(L):
     code = ctypes.c_int(7)
     assert L.fos_workspace_error(None, None, ctypes.byref(code)) == fos.FOS_ERR_INVALID_ARG
@@ -325,7 +367,8 @@ def test_host_validation_fuzz_never_crashes(L):
     sizes = [-16, -1, 0, 1, 15, 16, 17, 32, 48, 4096, 1 << 40, (1 << 62)]
     ptrs = [None, FAKE, ctypes.c_void_p(0x10001), ctypes.c_void_p(0x10010)]
     for n in ("fos_quantize", "fos_dequantize", "fos_quantize_grouped", "fos_quantize_colwise",
-              "fos_swizzle_scales", "fos_check_tile_amax", "fos_mm", "fos_amax"):
+              "fos_swizzle_scales", "fos_check_tile_amax", "fos_mm", "fos_amax",
+              "fos_qdq_fused", "fos_qdq_fused_static"):
         getattr(L, n).restype = ctypes.c_int
     valid = set(range(6))
     for _ in range(400):
@@ -349,4 +392,13 @@ def test_host_validation_fuzz_never_crashes(L):
                      ctypes.byref(cfg), p[0], None),
             L.fos_amax(p[0], dt, R, C, rng.choice([0, 1, 4]), p[1], None),
         ]
+        n = rng.choice([-1, 0, 1, 2, 64, 65])
+        k = max(n, 1)
+        P = ctypes.c_void_p * k
+        xs, os_, am = (P(*[rng.choice(ptrs) for _ in range(k)]) for _ in range(3))
+        rr = (i64 * k)(*[rng.choice(sizes) for _ in range(k)])
+        cc = (i64 * k)(*[rng.choice(sizes) for _ in range(k)])
+        rcs.append(L.fos_qdq_fused_static(n, xs, os_, rr, cc, am, dt, ctypes.byref(cfg), None))
+        rcs.append(L.fos_qdq_fused(n, xs, os_, rr, cc, am, dt, ctypes.byref(cfg), p[5],
+                                   rng.choice([0, 256, 1 << 20]), None))
         assert all(rc in valid for rc in rcs), rcs
