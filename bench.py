@@ -39,6 +39,7 @@ ROWS, COLS = 8192, 4096
 ELEMS = ROWS * COLS
 BYTES_PER_ELEM = 2 + 0.5 + 1.0 / 16          # bf16 read, codes and scales written
 ALG_BYTES = int(ELEMS * BYTES_PER_ELEM)       # 85,983,232 per tensor
+CLOCK_WINDOW_S = 0.6  # replay loop after the timed region, for the clock record
 METRIC = "4over6 quantize HBM GB/s (% of GB300 peak) and elements/s, 8192x4096 bf16"
 WORKLOAD = ("activation quantize 8192x4096 bf16, batch of 4 families (F1-F4), 1x16 blocks, "
             "per-tensor amax computed on device (pipelined list), 4over6 MSE exact-FP32, E4M3 448")
@@ -371,6 +372,15 @@ def run_fos(args):
         b.record(stream)
     torch.cuda.synchronize()
     per_step = sorted(a.elapsed_time(b) for a, b in ev)
+    # Clock evidence: the timed region lasts a few ms, shorter than many
+    # NVML sampling periods, so the same step keeps replaying for another
+    # CLOCK_WINDOW_S seconds right after it and the clock record covers both.
+    t_loop0 = time.time()
+    while time.time() - t_loop0 < CLOCK_WINDOW_S:
+        for _ in range(100):
+            step()
+        torch.cuda.synchronize()
+    t_wall2 = time.time()
     # The dominant kernel, timed in its own loop right after: graphs of the
     # three overlapped stages (fos_quantize_overlap: encode tensor i, amax of
     # tensor i+1); each stage also carries its amax-clear memset, so the
@@ -381,7 +391,10 @@ def run_fos(args):
     g_st = _graph(stages)
     g_st.replay()
     pipe_ms = _time_events(g_st.replay, max(3, args.steps // 4), stream) / 3
-    clock_summary = clocks.summary(t_wall0, t_wall1)
+    clock_summary = clocks.summary(t_wall0, t_wall2)
+    if clock_summary.get("window") == "timed region":
+        clock_summary["window"] = ("timed region and a %.1f s replay loop of the same step right "
+                                   "after it" % CLOCK_WINDOW_S)
     ms = max_over_ranks(ms, dev)
     out = step_line(ms, ws, args.steps, args.warmup, peak)
     pipe_bytes = ALG_BYTES + ELEMS * 2  # encode of tensor i + amax read of tensor i+1

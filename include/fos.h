@@ -15,9 +15,9 @@
  * Conventions shared by every entry point
  *   - Data pointers (x, out, codes, scales, amax, offs, workspaces) are
  *     DEVICE pointers owned by the caller; the library never allocates, frees
- *     or keeps them (fos_qdq_fused_static uses one fixed array of its own,
- *     fos_mm a cuBLASLt handle per device).  Host-side arrays (the pointer /
- *     size lists of the list calls) are read during the call only.
+ *     or keeps them (fos_qdq_fused_static uses one fixed array of its
+ *     own).  Host-side arrays (the pointer / size lists of the list calls)
+ *     are read during the call only.
  *   - Tensors are row-major and contiguous: x is [rows, cols]; codes are
  *     [rows, cols/2] bytes, element 2j in the low nibble of byte j; scales are
  *     E4M3 bytes [rows, cols/16] (1x16) or [rows/16, cols/16] (16x16), plain
@@ -231,16 +231,17 @@ FOS_API fos_status fos_swizzle_scales(const uint8_t* scales, int64_t rows, int64
  * with 1x16 blocks (codes [M, K/2] and [N, K/2]) and their block scales put
  * into the tiled GEMM layout (fos_swizzle_scales); a_amax / b_amax are the
  * amaxes they were quantized with (a: [M] when cfg->granularity is
- * FOS_SCALE_ROW, else [1]; b: [1]).  The block-scaled product D runs as a
- * cuBLASLt NVFP4 GEMM (a library GEMM: fp32 accumulation, no workspace);
- * this library's epilogue then applies the global decode scales,
+ * FOS_SCALE_ROW, else [1]; b: [1]).  One launch of this library's kernel on
+ * the tensor cores (tcgen05 block-scaled E2M1 MMAs with UE4M3 scales, fp32
+ * accumulation in tensor memory) forms the block-scaled product D of each
+ * 128 x 128 output tile, and its epilogue applies the global decode scales
+ * before the single store,
  *   out[m][n] = (D[m][n] * g_a(m)) * g_b,  g = rn(1 / S),
- * S the global scale fos_quantize used (cfg->e4m3_bound).  Large products
- * run as several GEMMs over row chunks of a, each followed by the epilogue
- * while its output is still in L2.  out: fp32 [M, N]
- * row-major, 16-byte aligned, like all operands.  M and N multiples of 16,
- * K a multiple of 64; FOS_ERR_UNSUPPORTED when cuBLASLt offers no
- * algorithm.  The first call on a device creates its cuBLASLt handle.
+ * S the global scale fos_quantize used (cfg->e4m3_bound).  out: fp32
+ * [M, N] row-major, 16-byte aligned, like all operands.  M and N multiples
+ * of 16, K a multiple of 64.  The kernel's waits are bounded: a tile whose
+ * wait gave up (which takes about a second) has NaN in its first element.
+ * Nothing is allocated.
  */
 FOS_API fos_status fos_mm(const uint8_t* a_codes, const uint8_t* a_scales_tiled,
                           const float* a_amax, const uint8_t* b_codes,

@@ -35,8 +35,12 @@ enum {
     /* in f32[n] (n even) -> out u16[n]: binary16 bits (RN), pairwise. */
     FOS_DIAG_F16_BITS = 6,
     /* in f32[n] -> out f32[n]: the block-scale quotient t / 6, correctly
-     * rounded, as the kernels compute it. */
-    FOS_DIAG_DIV6 = 7
+     * rounded (Markstein's correction where the quotient is normal). */
+    FOS_DIAG_DIV6 = 7,
+    /* in f32[n] (t = block amax * S, t >= 0) -> out u16[n]: the two E4M3
+     * block-scale codes the kernels derive from t, map-to-6 (E4M3 of t / 6)
+     * in the low byte and map-to-4 (E4M3 of t / 4) in the high byte. */
+    FOS_DIAG_SCALE_CODES = 8
 };
 
 /* fos_diag_convert -- applies `op` to n elements of the device buffer `in`

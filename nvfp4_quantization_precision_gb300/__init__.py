@@ -438,6 +438,7 @@ def quantize_grouped(x, offs, cfg=Config(), group_amax=None, codes=None, scales=
 
 DIAG_E2M1_ENCODE, DIAG_E2M1_DECODE, DIAG_E4M3_ENCODE, DIAG_E4M3_DECODE = 0, 1, 2, 3
 DIAG_F16_ROUND, DIAG_BF16_BITS, DIAG_F16_BITS, DIAG_DIV6 = 4, 5, 6, 7
+DIAG_SCALE_CODES = 8
 
 
 def diag_convert(op, inp, out):

@@ -68,8 +68,7 @@ def build(force=False, verbose=False, jobs=None, extra_flags=()):
             if err.strip():
                 print(err)
     tmp = LIB + ".tmp%d" % os.getpid()
-    cmd = [_nvcc(), *ARCH, "-shared", "-cudart", "static", "-o", tmp] + [o for o, _ in results] + [
-        "-lcublasLt"]
+    cmd = [_nvcc(), *ARCH, "-shared", "-cudart", "static", "-o", tmp] + [o for o, _ in results]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError("link failed:\n%s\n%s" % (" ".join(cmd), r.stderr))

@@ -53,6 +53,9 @@ __global__ void k_diag(int op, const void* in, void* out, int64_t n) {
             case FOS_DIAG_DIV6:
                 static_cast<float*>(out)[i] = div6_rn(fi[i]);
                 break;
+            case FOS_DIAG_SCALE_CODES:
+                static_cast<uint16_t*>(out)[i] = (uint16_t)scale_codes(fi[i], 1.0f);
+                break;
             default:
                 break;
         }

@@ -635,7 +635,7 @@ fos_status fos_qdq(int n, const void* const* x, void* const* out, const int64_t*
 }
 
 fos_status fos_diag_convert(int op, const void* in, void* out, int64_t n, fos_stream_t stream) {
-    if (op < FOS_DIAG_E2M1_ENCODE || op > FOS_DIAG_DIV6) return FOS_ERR_INVALID_ARG;
+    if (op < FOS_DIAG_E2M1_ENCODE || op > FOS_DIAG_SCALE_CODES) return FOS_ERR_INVALID_ARG;
     if (n < 0) return FOS_ERR_INVALID_ARG;
     if (n == 0) return FOS_OK;
     if (!in || !out) return FOS_ERR_INVALID_ARG;
@@ -883,9 +883,9 @@ fos_status fos_mm(const uint8_t* a_codes, const uint8_t* a_scales_tiled, const f
     }
     const int rc = run_mm(a_codes, a_scales_tiled, a_amax, cfg->granularity == FOS_SCALE_ROW,
                           b_codes, b_scales_tiled, b_amax, M, N, K,
-                          6.0f * (float)cfg->e4m3_bound, out, dev,
+                          6.0f * (float)cfg->e4m3_bound, out,
                           reinterpret_cast<cudaStream_t>(stream));
-    return rc == 0 ? FOS_OK : (rc == 1 ? FOS_ERR_UNSUPPORTED : FOS_ERR_CUDA);
+    return rc == 0 ? FOS_OK : FOS_ERR_CUDA;
 }
 
 }  // extern "C"

@@ -311,7 +311,9 @@ __device__ __forceinline__ void build_table(float2* tbl, float S, int lane) {
 
 // The common-scale table filled by a whole CTA of kThreads = 256 threads,
 // one division each: thread t < 128 writes r of code t, thread 128 + t
-// writes d of code t.
+// writes d of code t.  One table per CTA costs a CTA barrier but an eighth
+// of the divisions of per-warp tables (which also cost instruction issue
+// at the start of every launch).
 __device__ __forceinline__ void fill_table_cta(float2* tbl, float S, int tid) {
     const int c = tid & 127;
     const float sig = e4m3_f32((uint32_t)c);
@@ -443,38 +445,60 @@ __device__ __forceinline__ float div6_rn(float t) {
     return fdiv(t, 6.0f);
 }
 
+// t / 6 where only its E4M3 code is used (the map-to-6 block scale), for
+// t >= 0 or +Inf, without a branch: the same Markstein sequence as div6_rn,
+// which is correctly rounded wherever the quotient is a normal number.  Below
+// that (t < 6 * 2^-126) the quotient can be off in its last bits, but any
+// value under 2^-10 encodes to the E4M3 code 0, so the code is unchanged;
+// +Inf is clamped to FLT_MAX, whose quotient also saturates to 448.  (t is
+// never NaN: the block amax drops NaN and S is finite.)  Checked against
+// the code of the correctly rounded quotient for every non-negative float.
+__device__ __forceinline__ float div6_for_code(float t) {
+    constexpr float kInv6 = 0x1.555556p-3f;  // rn(1/6)
+    const float c = fminf(t, kFltMax);
+    const float q = fmul(c, kInv6);
+    const float r = __fmaf_rn(-q, 6.0f, c);
+    return __fmaf_rn(r, kInv6, q);
+}
+
 // Block-scale codes of the two candidates for a block (tile) amax:
 // s_k = (amax * S) / k, E4M3 RN satfinite.  Low byte: map-to-6, high byte:
-// map-to-4 (t / 4 is the exact product t * 0.25).
+// map-to-4 (t / 4 is the exact product t * 0.25).  Both forms of t / 6 give
+// the same codes for every t (checked exhaustively); which one a kernel uses
+// is a code-generation choice made per kernel by measurement: DIV_BRANCH
+// takes div6_rn (a branch to the full division outside the normal range),
+// otherwise the branch-free div6_for_code.
+template <bool DIV_BRANCH = false>
 __device__ __forceinline__ uint32_t scale_codes(float amax, float S) {
     const float t = fmul(amax, S);
-    return e4m3x2(div6_rn(t), fmul(t, 0.25f));
+    if constexpr (DIV_BRANCH) return e4m3x2(div6_rn(t), fmul(t, 0.25f));
+    else return e4m3x2(div6_for_code(t), fmul(t, 0.25f));
 }
 
 // Full 1x16 block: returns codes (2 words), the E4M3 scale byte, and with
 // OT != NONE the 8 output words of the selected candidate's decode.
-template <Err EM, Out OT>
+template <Err EM, Out OT, bool DB = false>
 __device__ __forceinline__ void encode_block_amax(const uint64_t (&xp)[8], float block_amax,
                                                   float S, const float2* tbl, uint64_t nz,
                                                   uint32_t (&code)[2], uint32_t& scale,
                                                   uint32_t (&out)[8]);
 
-template <Err EM, Out OT>
+template <Err EM, Out OT, bool DB = false>
 __device__ __forceinline__ void encode_block(const uint64_t (&xp)[8], float S,
                                              const float2* tbl, uint64_t nz,
                                              uint32_t (&code)[2], uint32_t& scale,
                                              uint32_t (&out)[8]) {
-    encode_block_amax<EM, OT>(xp, seg_amax(xp), S, tbl, nz, code, scale, out);
+    encode_block_amax<EM, OT, DB>(xp, seg_amax(xp), S, tbl, nz, code, scale, out);
 }
 
-template <Err EM, Out OT>
+template <Err EM, Out OT, bool DB>
 __device__ __forceinline__ void encode_block_amax(const uint64_t (&xp)[8], float block_amax,
                                                   float S, const float2* tbl, uint64_t nz,
                                                   uint32_t (&code)[2], uint32_t& scale,
                                                   uint32_t (&out)[8]) {
     // Block scales are non-negative, so their codes are below 0x80; the mask
     // only keeps the table index in range by construction.
-    const uint32_t sc = scale_codes(block_amax, S);
+    const uint32_t sc = scale_codes<DB>(block_amax, S);
     const uint32_t c6 = sc & 0xFFu;
     const float2 rd6 = tbl[c6 & 0x7Fu];
     if constexpr (EM == Err::STD) {
@@ -518,12 +542,12 @@ __device__ __forceinline__ float quad_tree(float p_r, float p_r8, int t) {
 
 // Both rows (r, r + 8) a lane holds of one 16x16 tile: codes of each row and
 // the tile's E4M3 scale byte.  Every lane of the warp must take part.
-template <Err EM>
+template <Err EM, bool DB = false>
 __device__ __forceinline__ void encode_tile_rows(const uint64_t (&x0)[8], const uint64_t (&x1)[8],
                                                  float S, const float2* tbl, uint64_t nz, int t,
                                                  uint32_t (&k0)[2], uint32_t (&k1)[2],
                                                  uint32_t& scale) {
-    const uint32_t sc = scale_codes(quad_max(fmaxf(seg_amax(x0), seg_amax(x1))), S);
+    const uint32_t sc = scale_codes<DB>(quad_max(fmaxf(seg_amax(x0), seg_amax(x1))), S);
     const uint32_t c6 = sc & 0xFFu;
     const float2 rd6 = tbl[c6 & 0x7Fu];
     uint32_t dummy[8];

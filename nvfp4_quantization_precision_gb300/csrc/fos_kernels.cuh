@@ -48,6 +48,12 @@ struct QdqTensor {
 };
 
 constexpr int kQdqMaxList = 64;
+constexpr int kQdqCtaTables = 16;  // QDQ lists up to this long keep all tables per CTA
+
+// Dynamic shared memory of the QDQ list kernel: its common-scale tables.
+inline size_t qdq_table_bytes(int n) {
+    return (size_t)(n <= kQdqCtaTables ? n : kWarps) * 128 * 8;
+}
 
 struct QdqArgs {
     int n;
@@ -120,13 +126,11 @@ template <In IT, Err EM, int kBuf = kTensorBuf>
 __global__ void __launch_bounds__(kThreads, min_ctas<EM>()) k_quant1x16_tensor(const EncArgs a) {
     chain_wait();
     chain_release();
-    __shared__ float2 s_tbl[kWarps][128];
+    __shared__ float2 tbl[128];  // one common-scale table for the CTA
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    float2* tbl = s_tbl[warp];
     const uint64_t nz = pk(a.neg_zero, a.neg_zero);
     const int64_t nw = (int64_t)gridDim.x * kWarps;
     const int64_t u = (int64_t)blockIdx.x * kWarps + warp;
-    if (u >= a.units) return;
     constexpr int64_t kBytes = (IT == In::F32) ? 64 : 32;
     const char* xb = static_cast<const char*>(a.x);
     // kBuf register buffers rotate over consecutive grid-stride units: unit i
@@ -142,7 +146,9 @@ __global__ void __launch_bounds__(kThreads, min_ctas<EM>()) k_quant1x16_tensor(c
         load_if<IT, kEncHint>(buf[k], xb + bk * kBytes, bk < a.nblk);
     }
     const float S = global_scale(a.amax[0], a.six_bound);
-    build_table(tbl, S, lane);
+    fill_table_cta(tbl, S, threadIdx.x);
+    __syncthreads();
+    if (u >= a.units) return;
     uint32_t dummy[8];
     // Steady state: while every unit this step loads or encodes is whole
     // (the test is on the unit's first block, the same for the whole warp),
@@ -242,7 +248,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas<EM>()) k_quant1x16(const En
                 uint64_t xp[8];
                 widen<IT>(cur, xp);
                 uint32_t code[2], scale;
-                encode_block<EM, Out::NONE>(xp, S, tbl, nz, code, scale, dummy);
+                encode_block<EM, Out::NONE, SRC == Src::GROUP>(xp, S, tbl, nz, code, scale, dummy);
                 const int64_t b = cc.row * a.nb + j;
                 st64(a.codes + b * 8, code[0], code[1]);
                 st8(a.scales + b, scale);
@@ -264,7 +270,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas<EM>()) k_quant1x16(const En
                 uint64_t xp[8];
                 widen<IT>(cur, xp);
                 uint32_t code[2], scale;
-                encode_block<EM, Out::NONE>(xp, S, tbl, nz, code, scale, dummy);
+                encode_block<EM, Out::NONE, SRC == Src::GROUP>(xp, S, tbl, nz, code, scale, dummy);
                 st64(a.codes + b * 8, code[0], code[1]);
                 st8(a.scales + b, scale);
             } else {  // zero-extended tail of a padded grouped tensor
@@ -372,19 +378,31 @@ __global__ void __launch_bounds__(kThreads, min_ctas<EM>()) k_qdq1x16(const __gr
     chain_release();
     static_assert(IT != In::F32, "fused QDQ is bf16 / fp16 only");
     constexpr Out OT = (IT == In::BF16) ? Out::BF16 : Out::F16;
-    __shared__ float2 s_tbl[kWarps][128];
+    // Common-scale tables (dynamic shared memory, qdq_table_bytes): a list of
+    // up to kQdqCtaTables tensors gets every tensor's table filled once per
+    // CTA at the start (about n divisions per thread); a longer list keeps
+    // one table per warp, rebuilt when the warp moves into the next tensor.
+    extern __shared__ float2 s_tbls[];
+    __shared__ float s_S[kQdqCtaTables];
+    const bool cta_tables = a.n <= kQdqCtaTables;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    float2* tbl = s_tbl[warp];
     const uint64_t nz = pk(a.neg_zero, a.neg_zero);
     const int64_t nw = (int64_t)gridDim.x * kWarps;
     int64_t u = (int64_t)blockIdx.x * kWarps + warp;
-    if (u >= a.units) return;
     int t = 0;
     while (t < a.n && a.t[t + 1].unit_begin <= u) ++t;
     int64_t b = (u - a.t[t].unit_begin) * 32 + lane;
-    bool v = b < a.t[t].nblk;
-    Raw<IT> cur;
+    bool v = u < a.units && b < a.t[t].nblk;
+    Raw<IT> cur;  // the first load goes out before the tables are filled
     load_if<IT, kQdqHint>(cur, static_cast<const char*>(a.t[t].x) + b * 32, v);
+    if (cta_tables) {
+        if ((int)threadIdx.x < a.n) s_S[threadIdx.x] = global_scale(*a.t[threadIdx.x].amax, a.six_bound);
+        __syncthreads();
+        for (int i = 0; i < a.n; ++i) fill_table_cta(s_tbls + 128 * i, s_S[i], threadIdx.x);
+        __syncthreads();
+    }
+    float2* tbl = s_tbls + 128 * warp;
+    if (u >= a.units) return;
     int ti = -1;
     float S = 1.0f;
     for (; u < a.units; u += nw) {
@@ -397,14 +415,19 @@ __global__ void __launch_bounds__(kThreads, min_ctas<EM>()) k_qdq1x16(const __gr
         load_if<IT, kQdqHint>(nxt, static_cast<const char*>(a.t[tn].x) + bn * 32, vn);
         if (t != ti) {
             ti = t;
-            S = global_scale(*a.t[t].amax, a.six_bound);
-            build_table(tbl, S, lane);
+            if (cta_tables) {
+                S = s_S[t];
+                tbl = s_tbls + 128 * t;
+            } else {
+                S = global_scale(*a.t[t].amax, a.six_bound);
+                build_table(tbl, S, lane);
+            }
         }
         if (v) {
             uint64_t xp[8];
             widen<IT>(cur, xp);
             uint32_t code[2], scale, out[8];
-            encode_block<EM, OT>(xp, S, tbl, nz, code, scale, out);
+            encode_block<EM, OT, EM == Err::STD>(xp, S, tbl, nz, code, scale, out);
             st256(static_cast<char*>(a.t[t].out) + b * 32, out);
         }
         cur = nxt;
@@ -526,12 +549,11 @@ __global__ void __launch_bounds__(kThreads, min_ctas<EM>())
     // launch reserves 128 spare bytes for this)
     unsigned char* s_buf = s_dyn + ((128u - (smem_u32(s_dyn) & 127u)) & 127u);
     __shared__ __align__(8) uint64_t s_bar[2];
-    __shared__ float2 s_tbl[kWarps][128];
+    __shared__ float2 tbl[128];  // one common-scale table for the CTA
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    float2* tbl = s_tbl[warp];
     const uint64_t nz = pk(a.neg_zero, a.neg_zero);
     const float S = global_scale(a.amax[0], a.six_bound);
-    build_table(tbl, S, lane);
+    fill_table_cta(tbl, S, tid);  // ordered before use by the barrier below
     if (tid == 0) {
         mbar_init(&s_bar[0], 1);
         mbar_init(&s_bar[1], 1);
@@ -726,11 +748,10 @@ __global__ void __launch_bounds__(kThreads, min_ctas<EM>())
     static_assert(IT != In::F32, "fused QDQ is bf16 / fp16 only");
     constexpr Out OT = (IT == In::BF16) ? Out::BF16 : Out::F16;
     constexpr int64_t kBytes = 32;
-    __shared__ float2 s_tbl[kWarps][128];
+    __shared__ float2 tbl[128];  // the current tensor's common-scale table, one per CTA
     __shared__ float s_red[kWarps];
     __shared__ float s_amax;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    float2* tbl = s_tbl[warp];
     const uint64_t nz = pk(a.q.neg_zero, a.q.neg_zero);
     const int64_t nw = (int64_t)gridDim.x * kWarps;
     const int64_t step = nw * 32;
@@ -754,7 +775,10 @@ __global__ void __launch_bounds__(kThreads, min_ctas<EM>())
         if (A < 0.0f) return;  // the wait gave up (the whole CTA leaves); failure recorded
         if (blockIdx.x == 0 && threadIdx.x == 0) *a.amax_out[s] = A;
         const float S = global_scale(A, a.q.six_bound);
-        build_table(tbl, S, lane);
+        // every warp of the CTA is past the previous tensor (fused_wait ends
+        // with a CTA barrier), so the one table can be refilled
+        fill_table_cta(tbl, S, threadIdx.x);
+        __syncthreads();
         const QdqTensor& T = a.q.t[s];
         const char* xb = static_cast<const char*>(T.x);
         char* ob = static_cast<char*>(T.out);
@@ -808,8 +832,13 @@ __global__ void __launch_bounds__(kThreads, tile_min_ctas<IT>()) k_quant16x16(co
     __shared__ float2 s_tbl[kWarps][128];
     if constexpr (SRC == Src::GROUP) load_group_ends(s_ends, a.offs, a.G, a.rows);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    float2* tbl = s_tbl[warp];
+    // per tensor: one table for the CTA; otherwise one per warp
+    float2* tbl = (SRC == Src::TENSOR) ? s_tbl[0] : s_tbl[warp];
     const uint64_t nz = pk(a.neg_zero, a.neg_zero);
+    if constexpr (SRC == Src::TENSOR) {  // filled before any warp can leave
+        fill_table_cta(tbl, global_scale(a.amax[0], a.six_bound), threadIdx.x);
+        __syncthreads();
+    }
     // One table per tensor: a grid-stride walk (the whole grid sweeps one
     // window at a time).  Per-row / per-group scales: each CTA walks its own
     // contiguous range, warps interleaved, so a warp's scale changes rarely.
@@ -844,10 +873,7 @@ __global__ void __launch_bounds__(kThreads, tile_min_ctas<IT>()) k_quant16x16(co
         while (g < a.G && cc.row * 16 >= s_ends[g]) ++g;
     int64_t key = -1;
     float S = 1.0f;
-    if constexpr (SRC == Src::TENSOR) {
-        S = global_scale(a.amax[0], a.six_bound);
-        build_table(tbl, S, lane);
-    }
+    if constexpr (SRC == Src::TENSOR) S = global_scale(a.amax[0], a.six_bound);
     int64_t u = u0;
     const bool quads_whole = (a.nb & 3) == 0;  // every band is whole tile quads
     for (; u < c1; u += ustep) {
@@ -894,7 +920,7 @@ __global__ void __launch_bounds__(kThreads, tile_min_ctas<IT>()) k_quant16x16(co
                 widen<IT>(cur0, x0);
                 widen<IT>(cur1, x1);
                 uint32_t k0[2], k1[2], scale;
-                encode_tile_rows<EM>(x0, x1, S, tbl, nz, t, k0, k1, scale);
+                encode_tile_rows<EM, SRC != Src::TENSOR>(x0, x1, S, tbl, nz, t, k0, k1, scale);
                 st64(c0, k0[0], k0[1]);
                 st64(c0 + 8 * (cols / 2), k1[0], k1[1]);
                 if (r == 0) st8(a.scales + cc.row * a.nb + J, scale);
@@ -922,7 +948,7 @@ __global__ void __launch_bounds__(kThreads, tile_min_ctas<IT>()) k_quant16x16(co
             widen<IT>(cur0, x0);  // zeros past the last tile of the band
             widen<IT>(cur1, x1);
             uint32_t k0[2], k1[2], scale;
-            encode_tile_rows<EM>(x0, x1, S, tbl, nz, t, k0, k1, scale);  // all lanes take part
+            encode_tile_rows<EM, SRC != Src::TENSOR>(x0, x1, S, tbl, nz, t, k0, k1, scale);  // all lanes take part
             if (J < a.nb) {
                 st64(c0, k0[0], k0[1]);
                 st64(c8, k1[0], k1[1]);
@@ -965,11 +991,10 @@ __global__ void __launch_bounds__(kThreads, min_ctas<EM>()) k_quant1x16_pipe(con
     chain_wait();
     chain_release();
     if (p.clear && blockIdx.x == 0 && threadIdx.x == 0) *p.clear = 0.0f;
-    __shared__ float2 s_tbl[kWarps][128];
+    __shared__ float2 tbl[128];  // one common-scale table for the CTA
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     constexpr int64_t kBytes = (IT == In::F32) ? 64 : 32;
     const EncArgs& a = p.enc;
-    float2* tbl = s_tbl[warp];
     const uint64_t nz = pk(a.neg_zero, a.neg_zero);
     const int64_t nw = (int64_t)gridDim.x * kWarps;
     const int64_t u = (int64_t)blockIdx.x * kWarps + warp;
@@ -981,7 +1006,8 @@ __global__ void __launch_bounds__(kThreads, min_ctas<EM>()) k_quant1x16_pipe(con
     Raw<IT> buf[2];
     load_if<IT, kEncHint>(buf[0], xb + b0 * kBytes, b0 < a.nblk);
     const float S = global_scale(a.amax[0], a.six_bound);
-    build_table(tbl, S, lane);
+    fill_table_cta(tbl, S, threadIdx.x);
+    __syncthreads();
     uint32_t dummy[8];
     float m = 0.0f;
     for (int64_t b = b0; b < nmax + lane; b += 2 * step) {  // b - lane: first block of unit
@@ -997,7 +1023,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas<EM>()) k_quant1x16_pipe(con
                 uint64_t xp[8];
                 widen<IT>(buf[k], xp);
                 uint32_t code[2], scale;
-                encode_block<EM, Out::NONE>(xp, S, tbl, nz, code, scale, dummy);
+                encode_block<EM, Out::NONE, true>(xp, S, tbl, nz, code, scale, dummy);
                 st64(a.codes + bc * 8, code[0], code[1]);
                 st8(a.scales + bc, scale);
             }
@@ -1029,8 +1055,11 @@ __global__ void __launch_bounds__(kThreads) k_dequant(const DeqArgs a) {
         // one scale for the tensor: the blocks are walked grid-stride as one
         // flat sequence (codes and outputs are block-major; a 1x16 scale is
         // per block, a 16x16 scale per (row / 16, block)), with the next
-        // block's code word and scale byte loaded a step ahead
-        build_table(tbl, global_scale(a.amax[0], a.six_bound), lane);
+        // block's code word and scale byte loaded a step ahead; one table
+        // for the CTA
+        tbl = s_tbl[0];
+        fill_table_cta(tbl, global_scale(a.amax[0], a.six_bound), threadIdx.x);
+        __syncthreads();
         const int64_t nblk = a.rows * a.nb, step = nw * 32;
         int64_t b = gw * 32 + lane;
         // 16x16: (row, column block) of b, advanced by step each iteration

@@ -127,7 +127,7 @@ cudaError_t launch_diag(int op, const void* in, void* out, int64_t n, cudaStream
 cudaError_t launch_wait_timeout(int which, uint32_t* word, cudaStream_t);
 int run_mm(const uint8_t* a_codes, const uint8_t* a_scales, const float* a_amax, int a_row,
            const uint8_t* b_codes, const uint8_t* b_scales, const float* b_amax, int64_t M,
-           int64_t N, int64_t K, float six_bound, float* out, int dev, cudaStream_t s);
+           int64_t N, int64_t K, float six_bound, float* out, cudaStream_t s);
 cudaError_t launch_swizzle(const uint8_t* scales, int64_t rows, int64_t nb, uint8_t* out,
                            cudaStream_t);
 cudaError_t launch_check_tile_amax(const float* amax, int64_t rows, int64_t* bad, cudaStream_t);

@@ -6,15 +6,15 @@ namespace fos {
 template <In IT>
 static cudaError_t by_err(Err em, const QdqArgs& a, cudaStream_t s) {
     switch (em) {
-        case Err::STD: return launch_persistent(k_qdq1x16<IT, Err::STD>, a, a.units, 0, s);
-        case Err::MAE: return launch_persistent(k_qdq1x16<IT, Err::MAE>, a, a.units, 0, s);
-        case Err::MSE: return launch_persistent(k_qdq1x16<IT, Err::MSE>, a, a.units, 0, s);
-        case Err::MAE_H: return launch_persistent(k_qdq1x16<IT, Err::MAE_H>, a, a.units, 0, s);
-        case Err::MSE_H: return launch_persistent(k_qdq1x16<IT, Err::MSE_H>, a, a.units, 0, s);
-        case Err::MAE_S: return launch_persistent(k_qdq1x16<IT, Err::MAE_S>, a, a.units, 0, s);
-        case Err::MSE_S: return launch_persistent(k_qdq1x16<IT, Err::MSE_S>, a, a.units, 0, s);
-        case Err::MAE_HS: return launch_persistent(k_qdq1x16<IT, Err::MAE_HS>, a, a.units, 0, s);
-        case Err::MSE_HS: return launch_persistent(k_qdq1x16<IT, Err::MSE_HS>, a, a.units, 0, s);
+        case Err::STD: return launch_persistent(k_qdq1x16<IT, Err::STD>, a, a.units, qdq_table_bytes(a.n), s);
+        case Err::MAE: return launch_persistent(k_qdq1x16<IT, Err::MAE>, a, a.units, qdq_table_bytes(a.n), s);
+        case Err::MSE: return launch_persistent(k_qdq1x16<IT, Err::MSE>, a, a.units, qdq_table_bytes(a.n), s);
+        case Err::MAE_H: return launch_persistent(k_qdq1x16<IT, Err::MAE_H>, a, a.units, qdq_table_bytes(a.n), s);
+        case Err::MSE_H: return launch_persistent(k_qdq1x16<IT, Err::MSE_H>, a, a.units, qdq_table_bytes(a.n), s);
+        case Err::MAE_S: return launch_persistent(k_qdq1x16<IT, Err::MAE_S>, a, a.units, qdq_table_bytes(a.n), s);
+        case Err::MSE_S: return launch_persistent(k_qdq1x16<IT, Err::MSE_S>, a, a.units, qdq_table_bytes(a.n), s);
+        case Err::MAE_HS: return launch_persistent(k_qdq1x16<IT, Err::MAE_HS>, a, a.units, qdq_table_bytes(a.n), s);
+        case Err::MSE_HS: return launch_persistent(k_qdq1x16<IT, Err::MSE_HS>, a, a.units, qdq_table_bytes(a.n), s);
     }
     return cudaErrorInvalidValue;
 }

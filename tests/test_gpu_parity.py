@@ -451,6 +451,34 @@ def test_diag_div6_exhaustive_against_ieee_division():
     assert mism == 0
 
 
+def test_diag_scale_codes_exhaustive():
+    """The two block-scale codes the kernels derive from t = block amax * S
+    (a branch-free t / 6 that is correctly rounded wherever the quotient is
+    normal, and the exact t / 4) equal the E4M3 codes of the correctly
+    rounded quotients t / 6 and t / 4, for every non-negative float32 t and
+    +Inf.  The quotient t / 6 comes from binary64 division rounded once to
+    binary32 (exact, see the division test above); both quotients are
+    encoded by the pinned E4M3 conversion."""
+    chunk = 1 << 28
+    end = 0x7F800001  # +0 .. +Inf
+    mism = 0
+    for start in range(0, end, chunk):
+        stop = min(end, start + chunk)
+        t = torch.arange(start, stop, dtype=torch.int64, device=DEV).to(torch.int32).view(
+            torch.float32)
+        got = torch.empty(t.numel(), dtype=torch.int16, device=DEV)
+        fos.diag_convert(fos.DIAG_SCALE_CODES, t, got)
+        q = torch.empty(2 * t.numel(), dtype=torch.float32, device=DEV)
+        q[0::2] = (t.double() / 6.0).float()
+        q[1::2] = t * 0.25
+        codes = torch.empty(2 * t.numel(), dtype=torch.uint8, device=DEV)
+        fos.diag_convert(fos.DIAG_E4M3_ENCODE, q, codes)
+        ref = codes[0::2].to(torch.int32) | (codes[1::2].to(torch.int32) << 8)
+        mism += int(((got.to(torch.int32) & 0xFFFF) != ref).sum().item())
+        del t, got, q, codes, ref
+    assert mism == 0
+
+
 def test_diag_div6_is_correctly_rounded():
     v = _dense_f32(1 << 22, seed=3)
     got = _run_diag(fos.DIAG_DIV6, v, torch.float32).numpy()
