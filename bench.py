@@ -542,6 +542,16 @@ def _rows(fos, xs, stream, peak, only=None):
         ms = _graph_ms(rot(lambda i: fos.quantize(xs[i], fos.Config(row_scaled=True),
                                                   codes=codes, scales=scales)), R8, stream)
         rec("encode_row_scaled_with_amax_pass", ALG_BYTES, ms)
+        # 4/6 MSE writing the scales straight into the tiled GEMM layout
+        tiled = torch.empty(fos.lib().fos_swizzled_scales_bytes(ROWS, COLS), dtype=torch.uint8,
+                            device=dev)
+        for row in (False, True):
+            c = fos.Config(row_scaled=row, scale_tiled=True)
+            a = ra if row else am
+            ms = _graph_ms(rot(lambda i: fos.quantize(xs[i], c, amax=a[i], codes=codes,
+                                                      scales=tiled)), R8, stream)
+            rec("encode_tiled_scales_mse_448_" + ("row" if row else "tensor"), ALG_BYTES, ms)
+        del tiled
     if want("colwise"):
         # the column-wise operand (x^T) alone and with the row-wise result of
         # the same read, 4/6 MSE, amax given
@@ -555,7 +565,13 @@ def _rows(fos, xs, stream, peak, only=None):
                                                           scales_t=st_, codes=codes, scales=scales)),
                        R8, stream)
         rec("colwise_and_rowwise_8192x4096_bf16_mse", ELEMS * (2 + 2 * (0.5 + 1 / 16)), ms)
-        del ct, st_
+        stt = torch.empty(fos.lib().fos_swizzled_scales_bytes(COLS, ROWS), dtype=torch.uint8,
+                          device=dev)
+        ct_ = fos.Config(scale_tiled=True)
+        ms = _graph_ms(rot(lambda i: fos.quantize_colwise(xs[i], ct_, amax=am[i], codes_t=ct,
+                                                          scales_t=stt)), R8, stream)
+        rec("colwise_tiled_scales_8192x4096_bf16_mse", ALG_BYTES, ms)
+        del ct, st_, stt
     if want("qdq"):
         # a9: fused QDQ at the metric shape
         outs4 = [torch.empty_like(x) for x in xs]

@@ -77,6 +77,7 @@ enum { FOS_MAE = 0, FOS_MSE = 1 };
 enum { FOS_ERR_EXACT_F32 = 0, FOS_ERR_F16 = 1 };
 enum { FOS_SCALE_TENSOR = 0, FOS_SCALE_ROW = 1 };
 enum { FOS_ORDER_TREE = 0, FOS_ORDER_SEQ = 1 };
+enum { FOS_SCALES_PLAIN = 0, FOS_SCALES_TILED = 1 };
 
 /* The knobs the pages name (Megatron PR "Fuse NVFP4 fake-QAT quantize-
  * dequantize with CuTe DSL", numerical contract: standard NVFP4 plus 4over6
@@ -97,6 +98,19 @@ typedef struct {
                         *   (the Transformer Engine term order the Megatron PR
                         *   keeps, "Packed pair arithmetic"); 1x16 blocks only,
                         *   FOS_ERR_UNSUPPORTED with 16x16 in 4over6 mode.     */
+    int scale_layout;  /* where the quantize calls write the E4M3 block scales:
+                        * FOS_SCALES_PLAIN (0): row-major [rows, cols/16]
+                        *   ([rows/16, cols/16] for 16x16);
+                        * FOS_SCALES_TILED (1): straight into the tiled layout
+                        *   of block-scaled FP4 GEMMs that fos_swizzle_scales
+                        *   produces (fos_swizzled_scales_bytes(rows, cols)
+                        *   bytes, zero padding included), ready for fos_mm;
+                        *   1x16 blocks and fewer than 2^30 rows (of x, and
+                        *   of x^T for fos_quantize_colwise) only, else
+                        *   FOS_ERR_UNSUPPORTED (fos_quantize, fos_quantize_list,
+                        *   fos_quantize_overlap, fos_quantize_colwise); the
+                        *   grouped quantize and fos_dequantize take plain
+                        *   scales only and return FOS_ERR_UNSUPPORTED.     */
 } fos_config;
 
 /*

@@ -51,7 +51,7 @@ class FosConfig(ctypes.Structure):
     _fields_ = [("block", ctypes.c_int), ("mode", ctypes.c_int), ("err_metric", ctypes.c_int),
                 ("err_precision", ctypes.c_int), ("e4m3_bound", ctypes.c_int),
                 ("granularity", ctypes.c_int), ("amax_is_input", ctypes.c_int),
-                ("err_order", ctypes.c_int)]
+                ("err_order", ctypes.c_int), ("scale_layout", ctypes.c_int)]
 
 
 @dataclass(frozen=True)
@@ -64,11 +64,13 @@ class Config:
     bound: int = 448
     row_scaled: bool = False
     seq_order: bool = False  # sum a block's error terms in element order (1x16 only)
+    scale_tiled: bool = False  # write scales in the tiled GEMM layout (1x16 only)
 
     def c(self, amax_is_input):
         return FosConfig(int(self.block16x16), int(self.four_over_six), int(self.mse),
                          int(self.err_f16), int(self.bound), int(self.row_scaled),
-                         int(bool(amax_is_input)), int(self.seq_order))
+                         int(bool(amax_is_input)), int(self.seq_order),
+                         int(self.scale_tiled))
 
 
 _lib = None
@@ -98,6 +100,8 @@ def lib():
         L.fos_workspace_error.argtypes = [P, P, ctypes.POINTER(I)]
         L.fos_check_tile_amax.argtypes = [P, I64, P, P]
         L.fos_tile_amax_status.argtypes = [P, P]
+        L.fos_swizzled_scales_bytes.argtypes = [I64, I64]
+        L.fos_swizzled_scales_bytes.restype = ctypes.c_int64
         for n in ("fos_check_tile_amax", "fos_tile_amax_status", "fos_amax", "fos_quantize", "fos_quantize_list", "fos_quantize_overlap",
                   "fos_dequantize", "fos_qdq", "fos_qdq_fused", "fos_workspace_error",
                   "fos_quantize_grouped", "fos_diag_convert"):
@@ -149,6 +153,17 @@ def scales_shape(rows, cols, block16x16):
     return (rows // 16 if block16x16 else rows, cols // 16)
 
 
+def _scales_buffer(rows, cols, cfg, dev):
+    """The scale output of a quantize of [rows, cols] under cfg: [rows, cols/16]
+    (plain), or the flat tiled buffer of fos_swizzled_scales_bytes bytes."""
+    if cfg.scale_tiled:
+        nbytes = lib().fos_swizzled_scales_bytes(rows, cols)
+        if nbytes < 0:
+            raise ValueError("bad shape for tiled scales")
+        return torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    return torch.empty(scales_shape(rows, cols, cfg.block16x16), dtype=torch.uint8, device=dev)
+
+
 def check_tile_amax(amax, bad=None):
     """Number of 16-row tiles of a per-row amax [rows] whose entries are not
     all bitwise equal (fos_check_tile_amax); reads the count back, so it
@@ -185,7 +200,7 @@ def quantize(x, cfg=Config(), amax=None, codes=None, scales=None, amax_given=Non
     if codes is None:
         codes = torch.empty((R, C // 2), dtype=torch.uint8, device=dev)
     if scales is None:
-        scales = torch.empty(scales_shape(R, C, cfg.block16x16), dtype=torch.uint8, device=dev)
+        scales = _scales_buffer(R, C, cfg, dev)
     cc = cfg.c(given)
     _check(lib().fos_quantize(_p(x), _DT[x.dtype], R, C, ctypes.byref(cc), _p(amax), _p(codes),
                               _p(scales), _stream(x)), "fos_quantize")
@@ -212,8 +227,7 @@ def quantize_list(xs, cfg=Config(), amaxes=None, codes=None, scales=None, amax_g
         codes = [torch.empty((x.shape[0], x.shape[1] // 2), dtype=torch.uint8, device=dev)
                  for x in xs]
     if scales is None:
-        scales = [torch.empty(scales_shape(x.shape[0], x.shape[1], cfg.block16x16),
-                              dtype=torch.uint8, device=dev) for x in xs]
+        scales = [_scales_buffer(x.shape[0], x.shape[1], cfg, dev) for x in xs]
     P = ctypes.c_void_p * n
     xp = P(*[x.data_ptr() for x in xs])
     ap = P(*[a.data_ptr() for a in amaxes])
@@ -299,12 +313,12 @@ def quantize_colwise(x, cfg=Config(), amax=None, codes_t=None, scales_t=None, ro
     if codes_t is None:
         codes_t = torch.empty((C, R // 2), dtype=torch.uint8, device=dev)
     if scales_t is None:
-        scales_t = torch.empty((C, R // 16), dtype=torch.uint8, device=dev)
+        scales_t = _scales_buffer(C, R, cfg, dev)
     dual = rowwise or codes is not None or scales is not None
     if dual and codes is None:
         codes = torch.empty((R, C // 2), dtype=torch.uint8, device=dev)
     if dual and scales is None:
-        scales = torch.empty((R, C // 16), dtype=torch.uint8, device=dev)
+        scales = _scales_buffer(R, C, cfg, dev)
     L = lib()
     if not getattr(L, "_colwise_declared", False):
         P, I64, I = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int

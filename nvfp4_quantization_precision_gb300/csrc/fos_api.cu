@@ -37,8 +37,32 @@ fos_status check_config(const fos_config* cfg) {
     if (cfg->amax_is_input != 0 && cfg->amax_is_input != 1) return FOS_ERR_INVALID_ARG;
     if (cfg->err_order != FOS_ORDER_TREE && cfg->err_order != FOS_ORDER_SEQ)
         return FOS_ERR_INVALID_ARG;
+    if (cfg->scale_layout != FOS_SCALES_PLAIN && cfg->scale_layout != FOS_SCALES_TILED)
+        return FOS_ERR_INVALID_ARG;
     if (cfg->e4m3_bound != 448 && cfg->e4m3_bound != 256) return FOS_ERR_UNSUPPORTED;
     return FOS_OK;
+}
+
+bool tiled(const fos_config* cfg) { return cfg->scale_layout == FOS_SCALES_TILED; }
+
+// Scales in the tiled GEMM layout are written for 1x16 blocks and fewer than
+// 2^30 rows (the kernels keep block positions in 32 bits).
+fos_status check_layout(const fos_config* cfg, int64_t rows) {
+    if (tiled(cfg) && (cfg->block != FOS_BLOCK_1X16 || rows >= (INT64_C(1) << 30)))
+        return FOS_ERR_UNSUPPORTED;
+    return FOS_OK;
+}
+
+// 4-block tiles per tile-row of the tiled scale layout of [rows, cols].
+int64_t tiled_pc4(int64_t cols) { return (cols / 16 + 3) / 4; }
+
+// The tiled layout pads the scale matrix to whole 128 x 4 tiles; the padding
+// must read as zero scales, so when there is any the buffer is cleared
+// before the kernel writes the real scales.
+cudaError_t clear_tiled_padding(uint8_t* scales, int64_t rows, int64_t cols, cudaStream_t s) {
+    if (rows % 128 == 0 && (cols / 16) % 4 == 0) return cudaSuccess;
+    const size_t bytes = (size_t)((rows + 127) / 128 * 128) * (size_t)(tiled_pc4(cols) * 4);
+    return cudaMemsetAsync(scales, 0, bytes, s);
 }
 
 // The sequential term order is offered for 1x16 blocks (its source is a 1x16
@@ -198,6 +222,14 @@ cudaError_t run_quant(const void* x, fos_dtype dt, int64_t rows, int64_t cols,
     } else {
         a.cpr = (a.nb + 31) / 32;
         a.units = (src == Src::TENSOR) ? (a.nblk + 31) / 32 : rows * a.cpr;
+        if (tiled(cfg) && src != Src::GROUP) {
+            a.sc_pc4 = tiled_pc4(cols);
+            switch (it) {
+                case In::BF16: return launch_quant1x16_tl_bf16(em, src, a, s);
+                case In::F16: return launch_quant1x16_tl_f16(em, src, a, s);
+                case In::F32: return launch_quant1x16_tl_f32(em, src, a, s);
+            }
+        }
         switch (it) {
             case In::BF16: return launch_quant1x16_bf16(em, src, a, s);
             case In::F16: return launch_quant1x16_f16(em, src, a, s);
@@ -233,6 +265,15 @@ cudaError_t run_rowpass(const void* x, fos_dtype dt, int64_t rows, int64_t cols,
     a.neg_zero = -0.0f;
     a.amax_given = cfg->amax_is_input;
     const Err em = err_of(cfg);
+    if (tiled(cfg)) {
+        a.sc_pc4 = tiled_pc4(cols);
+        switch (in_of(dt)) {
+            case In::BF16: return launch_quant1x16_rowpass_tl_bf16(em, k, a, s);
+            case In::F16: return launch_quant1x16_rowpass_tl_f16(em, k, a, s);
+            case In::F32: return launch_quant1x16_rowpass_tl_f32(em, k, a, s);
+        }
+        return cudaErrorInvalidValue;
+    }
     switch (in_of(dt)) {
         case In::BF16: return launch_quant1x16_rowpass_bf16(em, k, a, s);
         case In::F16: return launch_quant1x16_rowpass_f16(em, k, a, s);
@@ -268,6 +309,10 @@ fos_status overlap_one(const void* x, fos_dtype dt, int64_t rows, int64_t cols,
             return cuda_status(run_amax_cleared(x_next, dt, rows_next, cols_next, amax_next, s));
         return FOS_OK;
     }
+    if (tiled(cfg)) {
+        st = cuda_status(clear_tiled_padding(scales, rows, cols, s));
+        if (st) return st;
+    }
     if (!next_live)
         return cuda_status(run_quant(x, dt, rows, cols, cfg, amax, Src::TENSOR, nullptr, 0, codes,
                                      scales, s));
@@ -289,6 +334,10 @@ fos_status overlap_one(const void* x, fos_dtype dt, int64_t rows, int64_t cols,
     p.aamax = amax_next;
     p.aseg = rows_next * (cols_next / 16);
     p.aunits = (p.aseg + 31) / 32;
+    if (tiled(cfg)) {
+        a.sc_pc4 = tiled_pc4(cols);
+        return cuda_status(launch_pipe_tl(in_of(dt), err_of(cfg), p, s));
+    }
     return cuda_status(launch_pipe(in_of(dt), err_of(cfg), p, s));
 }
 
@@ -298,6 +347,8 @@ fos_status check_quant_args(const void* x, int64_t rows, int64_t cols, const fos
     fos_status st = check_shape(rows, cols, cfg->block == FOS_BLOCK_16X16);
     if (st) return st;
     st = check_order(cfg);
+    if (st) return st;
+    st = check_layout(cfg, rows);
     if (st) return st;
     if (rows == 0 || cols == 0) {
         if (!cfg->amax_is_input && !(cfg->granularity == FOS_SCALE_ROW && rows == 0) && !amax)
@@ -350,6 +401,10 @@ fos_status quantize_one(const void* x, fos_dtype dt, int64_t rows, int64_t cols,
     if (rows == 0 || cols == 0) {  // nothing to encode; a computed amax is 0
         const size_t n = (src == Src::ROW) ? (size_t)rows : 1;
         return cuda_status(cudaMemsetAsync(amax, 0, sizeof(float) * n, s));
+    }
+    if (tiled(cfg)) {
+        const fos_status st = cuda_status(clear_tiled_padding(scales, rows, cols, s));
+        if (st) return st;
     }
     if (src == Src::ROW && cfg->block == FOS_BLOCK_1X16) {
         const int k = rowpass_k(cols / 16);
@@ -522,6 +577,7 @@ fos_status fos_quantize_grouped(const void* x, fos_dtype dt, int64_t rows, int64
     if (st) return st;
     st = check_order(cfg);
     if (st) return st;
+    if (tiled(cfg)) return FOS_ERR_UNSUPPORTED;  // grouped scales are plain
     if (G < 1) return FOS_ERR_INVALID_ARG;
     if (G > FOS_GROUPED_MAX_GROUPS) return FOS_ERR_UNSUPPORTED;
     if (!x || !offs || !group_amax || !codes || !scales) return FOS_ERR_INVALID_ARG;
@@ -548,6 +604,7 @@ fos_status fos_dequantize(const uint8_t* codes, const uint8_t* scales, const flo
     const bool b16 = cfg->block == FOS_BLOCK_16X16;
     st = check_shape(rows, cols, b16);
     if (st) return st;
+    if (tiled(cfg)) return FOS_ERR_UNSUPPORTED;  // decodes plain scales
     if (!codes || !scales || !amax || !out) return FOS_ERR_INVALID_ARG;
     if (!aligned(out, 32) || !aligned(codes, 8)) return FOS_ERR_MISALIGNED;
     const int dev = common_device({codes, scales, amax, out});
@@ -779,6 +836,8 @@ fos_status fos_quantize_colwise(const void* x, fos_dtype dt, int64_t rows, int64
     if (st) return st;
     st = check_shape(cols, rows, false);  // x^T: blocks run down the rows
     if (st) return st;
+    st = check_layout(cfg, rows > cols ? rows : cols);  // x^T has cols rows
+    if (st) return st;
     if ((codes == nullptr) != (scales == nullptr)) return FOS_ERR_INVALID_ARG;
     const bool dual = codes != nullptr;
     if (!amax) return FOS_ERR_INVALID_ARG;
@@ -822,6 +881,18 @@ fos_status fos_quantize_colwise(const void* x, fos_dtype dt, int64_t rows, int64
     a.tiles = ((rows + tile_r - 1) / tile_r) * a.tiles_c;
     a.six_bound = 6.0f * (float)cfg->e4m3_bound;
     a.neg_zero = -0.0f;
+    if (tiled(cfg)) {
+        // x^T is [cols, rows]: its scale matrix has cols rows of rows / 16 blocks
+        a.pc4_t = tiled_pc4(rows);
+        a.pc4 = tiled_pc4(cols);
+        st = cuda_status(clear_tiled_padding(scales_t, cols, rows, s));
+        if (st) return st;
+        if (dual) {
+            st = cuda_status(clear_tiled_padding(scales, rows, cols, s));
+            if (st) return st;
+        }
+        return cuda_status(launch_colwise_tl(in_of(dt), err_of(cfg), dual, a, s));
+    }
     return cuda_status(launch_colwise(in_of(dt), err_of(cfg), dual, a, s));
 }
 

@@ -574,6 +574,38 @@ __device__ __forceinline__ void encode_tile_rows(const uint64_t (&x0)[8], const 
     }
 }
 
+// Byte offset of the scale of block (row, j) (j = 16-column block of the
+// row) in the tiled layout block-scaled FP4 GEMMs read: the scale matrix
+// padded to 128-row x 4-block tiles of 512 bytes stored tile-row by
+// tile-row (pc4 tiles per tile-row), block (32 i + r, k) of a tile at byte
+// 16 r + 4 i + k.  Rows and blocks fit 31 bits and the tile index 32 bits
+// (the host admits tiled scales for rows < 2^30 only), so all but the final
+// scaling by 512 is 32-bit arithmetic.
+__device__ __forceinline__ int64_t tiled_scale_off(int32_t row, int32_t j, int32_t pc4) {
+    const uint32_t tile = (uint32_t)(row >> 7) * (uint32_t)pc4 + (uint32_t)(j >> 2);
+    return ((int64_t)tile << 9) + (int64_t)(((row & 31) << 4) | (((row >> 5) & 3) << 2) | (j & 3));
+}
+
+// Position (row, column block) of a block walked with a fixed stride in
+// blocks, kept up to date without a division per block (tiled scales; rows
+// below 2^30, so a position a few strides past the end still fits).
+struct BlockPos {
+    int32_t row = 0, col = 0;
+    __device__ __forceinline__ void init(int64_t b, int64_t nb) {
+        const int64_t r = b / nb;
+        row = (int32_t)r;
+        col = (int32_t)(b - r * nb);
+    }
+    __device__ __forceinline__ void advance(int32_t srow, int32_t scol, int32_t nb) {
+        col += scol;
+        row += srow;
+        if (col >= nb) {
+            col -= nb;
+            ++row;
+        }
+    }
+};
+
 // Balanced contiguous split of `units` work units over `parts` workers.
 __device__ __forceinline__ int64_t split_at(int64_t units, int64_t parts, int64_t i) {
     return (int64_t)(((unsigned __int128)units * (unsigned __int128)i) / (unsigned __int128)parts);

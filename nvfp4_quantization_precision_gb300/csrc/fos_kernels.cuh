@@ -37,7 +37,16 @@ struct EncArgs {
     float six_bound;       // 6 * E4M3 bound
     float neg_zero;        // -0.0f (run-time operand of mul2_nc)
     int amax_given;        // row pass: amax is an input (else computed, written)
+    int64_t sc_pc4;        // tiled scales: 4-block tiles per tile-row (kernels with TL)
 };
+
+// Scale byte index of block (row, j) = flat block b: the plain layout, or
+// with TL the tiled layout of block-scaled FP4 GEMMs.
+template <bool TL>
+__device__ __forceinline__ int64_t scale_at(int64_t b, int64_t row, int64_t j, int64_t pc4) {
+    if constexpr (TL) return tiled_scale_off((int32_t)row, (int32_t)j, (int32_t)pc4);
+    else return b;
+}
 
 struct QdqTensor {
     const void* x;
@@ -122,7 +131,7 @@ constexpr int tile_min_ctas() { return 2; }
 // ------------------------------------------------------------------------
 constexpr int kTensorBuf = 2;  // register buffers of the per-tensor encode (prefetch depth + 1)
 
-template <In IT, Err EM, int kBuf = kTensorBuf>
+template <In IT, Err EM, bool TL = false, int kBuf = kTensorBuf>
 __global__ void __launch_bounds__(kThreads, min_ctas<EM>()) k_quant1x16_tensor(const EncArgs a) {
     chain_wait();
     chain_release();
@@ -150,6 +159,15 @@ __global__ void __launch_bounds__(kThreads, min_ctas<EM>()) k_quant1x16_tensor(c
     __syncthreads();
     if (u >= a.units) return;
     uint32_t dummy[8];
+    // TL: (row, column block) of the block encoded next, advanced by one grid
+    // step per block
+    BlockPos pos;
+    int32_t srow = 0, scol = 0, nb32 = (int32_t)a.nb;
+    if constexpr (TL) {
+        pos.init(b0, a.nb);
+        srow = (int32_t)(step / a.nb);
+        scol = (int32_t)(step - (int64_t)srow * a.nb);
+    }
     // Steady state: while every unit this step loads or encodes is whole
     // (the test is on the unit's first block, the same for the whole warp),
     // loads and encodes go without bounds checks or branches; the guarded
@@ -166,7 +184,8 @@ __global__ void __launch_bounds__(kThreads, min_ctas<EM>()) k_quant1x16_tensor(c
             const int64_t bc = b + k * step;
             encode_block<EM, Out::NONE>(xp, S, tbl, nz, code, scale, dummy);
             st64(a.codes + bc * 8, code[0], code[1]);
-            st8(a.scales + bc, scale);
+            st8(a.scales + scale_at<TL>(bc, pos.row, pos.col, a.sc_pc4), scale);
+            if constexpr (TL) pos.advance(srow, scol, nb32);
         }
     }
     for (; b < a.nblk + lane; b += kBuf * step) {  // b - lane: first block of unit
@@ -181,8 +200,9 @@ __global__ void __launch_bounds__(kThreads, min_ctas<EM>()) k_quant1x16_tensor(c
                 uint32_t code[2], scale;
                 encode_block<EM, Out::NONE>(xp, S, tbl, nz, code, scale, dummy);
                 st64(a.codes + bc * 8, code[0], code[1]);
-                st8(a.scales + bc, scale);
+                st8(a.scales + scale_at<TL>(bc, pos.row, pos.col, a.sc_pc4), scale);
             }
+            if constexpr (TL) pos.advance(srow, scol, nb32);
         }
     }
 }
@@ -192,7 +212,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas<EM>()) k_quant1x16_tensor(c
 // contiguous range of (row, 32-block chunk) units so that the global scale
 // (and its table) changes only at row / group boundaries.
 // ------------------------------------------------------------------------
-template <In IT, Err EM, Src SRC>
+template <In IT, Err EM, Src SRC, bool TL = false>
 __global__ void __launch_bounds__(kThreads, min_ctas<EM>()) k_quant1x16(const EncArgs a) {
     chain_wait();
     chain_release();
@@ -251,7 +271,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas<EM>()) k_quant1x16(const En
                 encode_block<EM, Out::NONE, SRC == Src::GROUP>(xp, S, tbl, nz, code, scale, dummy);
                 const int64_t b = cc.row * a.nb + j;
                 st64(a.codes + b * 8, code[0], code[1]);
-                st8(a.scales + b, scale);
+                st8(a.scales + scale_at<TL>(b, cc.row, j, a.sc_pc4), scale);
                 cur = nxt;
                 cc = nc;
                 j = jn;
@@ -272,7 +292,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas<EM>()) k_quant1x16(const En
                 uint32_t code[2], scale;
                 encode_block<EM, Out::NONE, SRC == Src::GROUP>(xp, S, tbl, nz, code, scale, dummy);
                 st64(a.codes + b * 8, code[0], code[1]);
-                st8(a.scales + b, scale);
+                st8(a.scales + scale_at<TL>(b, cc.row, j, a.sc_pc4), scale);
             } else {  // zero-extended tail of a padded grouped tensor
                 st64(a.codes + b * 8, 0u, 0u);
                 st8(a.scales + b, 0u);
@@ -295,7 +315,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas<EM>()) k_quant1x16(const En
 // row in between and so finished reading it.  One barrier per row (table
 // ready) with the amax given, two with the amax computed (reduction, table).
 // ------------------------------------------------------------------------
-template <In IT, Err EM, int K>
+template <In IT, Err EM, int K, bool TL = false>
 __global__ void __launch_bounds__(kThreads) k_quant1x16_rowpass(const EncArgs a) {
     chain_wait();
     chain_release();
@@ -358,7 +378,7 @@ __global__ void __launch_bounds__(kThreads) k_quant1x16_rowpass(const EncArgs a)
                 encode_block_amax<EM, Out::NONE>(xp, bam[k], S, s_tbl[par], nz, code, scale, dummy);
                 const int64_t b = row * a.nb + j;
                 st64(a.codes + b * 8, code[0], code[1]);
-                st8(a.scales + b, scale);
+                st8(a.scales + scale_at<TL>(b, row, j, a.sc_pc4), scale);
             }
             cur[k] = nxt[k];
         }
@@ -473,6 +493,8 @@ struct ColArgs {
     int64_t tiles;
     float six_bound;
     float neg_zero;
+    int64_t pc4_t;      // tiled scales of x^T (TL): 4-block tiles per tile-row
+    int64_t pc4;        // tiled scales of x (TL, DUAL)
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -538,7 +560,7 @@ __device__ __forceinline__ void read_seg_smem(const unsigned char* p, Raw<IT>& r
     }
 }
 
-template <In IT, Err EM, bool DUAL>
+template <In IT, Err EM, bool DUAL, bool TL = false>
 __global__ void __launch_bounds__(kThreads, min_ctas<EM>())
     k_quant_colwise(const __grid_constant__ ColArgs a) {
     using T = ColTile<IT>;
@@ -610,7 +632,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas<EM>())
                     encode_block<EM, Out::NONE>(xp, S, tbl, nz, code, scale, dummy);
                     const int64_t blk = row * (a.cols / 16) + col / 16;
                     st64(a.codes + blk * 8, code[0], code[1]);
-                    st8(a.scales + blk, scale);
+                    st8(a.scales + scale_at<TL>(blk, row, col / 16, a.pc4), scale);
                 }
             }
         }
@@ -638,18 +660,21 @@ __global__ void __launch_bounds__(kThreads, min_ctas<EM>())
                     if (!whole) {
                         const int64_t blk = col * nb_t + row / 16;
                         st64(a.codes_t + blk * 8, code[0], code[1]);
-                        st8(a.scales_t + blk, scale);
+                        st8(a.scales_t + scale_at<TL>(blk, col, row / 16, a.pc4_t), scale);
                     }
                 }
             }
             if (whole) {
                 const int64_t blk = col * nb_t + r0 / 16;
+                // tiled: the kNB scales (kNB | 4, r0 / 16 a multiple of kNB) are
+                // consecutive bytes of one 4-byte group of the tile
+                const int64_t sidx = scale_at<TL>(blk, col, r0 / 16, a.pc4_t);
                 if constexpr (kNB == 4) {
                     st256(a.codes_t + blk * 8, cw);
-                    st32(a.scales_t + blk, sw);
+                    st32(a.scales_t + sidx, sw);
                 } else {
                     st128(a.codes_t + blk * 8, cw);
-                    st16(a.scales_t + blk, sw);
+                    st16(a.scales_t + sidx, sw);
                 }
             }
         }
@@ -986,7 +1011,7 @@ struct PipeArgs {
     int64_t aunits;        //             32-segment units
 };
 
-template <In IT, Err EM>
+template <In IT, Err EM, bool TL = false>
 __global__ void __launch_bounds__(kThreads, min_ctas<EM>()) k_quant1x16_pipe(const PipeArgs p) {
     chain_wait();
     chain_release();
@@ -1009,6 +1034,13 @@ __global__ void __launch_bounds__(kThreads, min_ctas<EM>()) k_quant1x16_pipe(con
     fill_table_cta(tbl, S, threadIdx.x);
     __syncthreads();
     uint32_t dummy[8];
+    BlockPos pos;  // TL: (row, column block) of block b + k * step, advanced per step
+    int32_t srow = 0, scol = 0, nb32 = (int32_t)a.nb;
+    if constexpr (TL) {
+        pos.init(b0, a.nb);
+        srow = (int32_t)(step / a.nb);
+        scol = (int32_t)(step - (int64_t)srow * a.nb);
+    }
     float m = 0.0f;
     for (int64_t b = b0; b < nmax + lane; b += 2 * step) {  // b - lane: first block of unit
 #pragma unroll
@@ -1025,8 +1057,9 @@ __global__ void __launch_bounds__(kThreads, min_ctas<EM>()) k_quant1x16_pipe(con
                 uint32_t code[2], scale;
                 encode_block<EM, Out::NONE, true>(xp, S, tbl, nz, code, scale, dummy);
                 st64(a.codes + bc * 8, code[0], code[1]);
-                st8(a.scales + bc, scale);
+                st8(a.scales + scale_at<TL>(bc, pos.row, pos.col, a.sc_pc4), scale);
             }
+            if constexpr (TL) pos.advance(srow, scol, nb32);
             uint64_t xq[8];
             widen<IT>(ra, xq);
             m = fmaxf(m, seg_amax(xq));

@@ -120,7 +120,16 @@ cudaError_t launch_quant16x16_f32(Err, Src, const EncArgs&, cudaStream_t);
 cudaError_t launch_qdq(In, Err, const QdqArgs&, cudaStream_t);
 cudaError_t launch_qdq_fused(In, Err, const QdqFusedArgs&, cudaStream_t);
 cudaError_t launch_colwise(In, Err, bool dual, const ColArgs&, cudaStream_t);
+// the same kernels writing their block scales in the tiled GEMM layout
+cudaError_t launch_quant1x16_tl_bf16(Err, Src, const EncArgs&, cudaStream_t);
+cudaError_t launch_quant1x16_tl_f16(Err, Src, const EncArgs&, cudaStream_t);
+cudaError_t launch_quant1x16_tl_f32(Err, Src, const EncArgs&, cudaStream_t);
+cudaError_t launch_quant1x16_rowpass_tl_bf16(Err, int k, const EncArgs&, cudaStream_t);
+cudaError_t launch_quant1x16_rowpass_tl_f16(Err, int k, const EncArgs&, cudaStream_t);
+cudaError_t launch_quant1x16_rowpass_tl_f32(Err, int k, const EncArgs&, cudaStream_t);
+cudaError_t launch_colwise_tl(In, Err, bool dual, const ColArgs&, cudaStream_t);
 cudaError_t launch_pipe(In, Err, const PipeArgs&, cudaStream_t);
+cudaError_t launch_pipe_tl(In, Err, const PipeArgs&, cudaStream_t);
 cudaError_t launch_dequant(Out, bool b16, Src, const DeqArgs&, cudaStream_t);
 cudaError_t launch_amax(In, Src, const AmaxArgs&, cudaStream_t);
 cudaError_t launch_diag(int op, const void* in, void* out, int64_t n, cudaStream_t);

@@ -4,30 +4,43 @@
 // in the epilogue (grouped PR, the dense-recipe commit's four_over_six_mm
 // forward; per row of a for a row-scaled a, the MoE commit's epilogue).
 //
-// One CTA computes one BM x BN tile of out.  Six warps:
-//   warp 0   (one thread)  TMA producer: per K stage of 256 elements, the a and
-//            b code tiles (2D TMA, 128-byte swizzle) and the stage's four
-//            512-byte scale atoms of each operand (1D bulk copies) into a
-//            ring of kStages shared-memory stages, completion on mbarriers;
-//   warp 1   allocates the tensor memory; one thread copies each stage's scale
-//            atoms into tensor memory (tcgen05.cp 32x128b.warpx4) and issues
-//            four tcgen05.mma kind::mxf4nvf4 block_scale scale_vec::4X
-//            (M = BM, N = BN, K = 64 each) accumulating in tensor memory,
-//            then frees the stage (tcgen05.commit to its mbarrier);
-//   warps 2-5 epilogue: wait for the last MMA, read the FP32 accumulator from
-//            tensor memory (tcgen05.ld, warp w reads lanes 32 (w % 4) ..),
-//            multiply by g_a(m) and then g_b, store.
+// A persistent kernel: one CTA per SM walks BM x BN = 128 x 256 output tiles
+// (tile t, t + grid, ...).  Warp roles:
+//   warp 0      (one thread) TMA producer: per K stage of 256 elements, the a
+//               and b code tiles (2D TMA, 128-byte swizzle) and the stage's
+//               512-byte scale atoms (1D bulk copies: four for a, four per
+//               128 rows of b) into a ring of kStages shared-memory stages;
+//   warp 1      allocates the tensor memory; one thread issues per stage four
+//               tcgen05.mma kind::mxf4nvf4 block_scale scale_vec::4X
+//               (M = 128, N = 256, K = 64 each) into the accumulator, then
+//               frees the stage (tcgen05.commit to its mbarrier) and, after a
+//               tile's last stage, hands the accumulator to the epilogue;
+//   warps 2-5   scale warps: move each stage's scale atoms from shared to
+//               tensor memory (ld.shared + tcgen05.st), warp w into the lanes
+//               32 (w % 4) .. 32 (w % 4) + 31 it may write;
+//   warps 6-..  epilogue (kEpi warps, kEpi / 4 per lane quadrant): read the
+//               FP32 accumulator (tcgen05.ld), multiply by g_a(m) and then
+//               g_b, stage 32 x 32 chunks in shared memory in the 128-byte
+//               swizzle and store them with TMA (cp.async.bulk.tensor), which
+//               clips the rows and columns past the end of out.
+// The accumulator (256 columns) and two scale buffers (48 columns each: a
+// stage's scales are written while the previous stage's MMAs read theirs)
+// take 352 of the 512 tensor-memory columns.
+//
 // Operands are K-major: a row of a (or b) holds K/2 code bytes, element 2j in
 // the low nibble of byte j, which is the element order of the E2M1 operand.
 // The scale atom of rows [128 t, 128 t + 128) and K elements [64 c, 64 c + 64)
 // is the 512-byte tile (t, c) of the tiled layout: byte 16 j + 4 i + k holds
-// the scale of row 32 i + j, 16-element block k.  Copied with the warpx4
-// shape, tensor-memory lane 32 q + j, column c0 + i then holds the four
-// scales of row 32 i + j for every q, where the MMA reads them.
+// the scale of row 32 i + j, 16-element block k.  The MMA reads the scales of
+// row r (of a, or of the 128-row half h of b) from tensor-memory lane
+// 32 q + r % 32, column c0 + r / 32 (+ 4 h for b), for each quadrant q: a
+// scale warp of quadrant q stores 16-byte row j of the atom (columns c0 ..
+// c0 + 3) to its lane 32 q + j, which is that content.
 //
 // Every mbarrier wait is bounded (about a second); a wait that gives up marks
-// the CTA failed, the CTA still drains what it issued and frees its tensor
-// memory, and the tile's first output element is set to NaN.
+// the CTA failed, the CTA still drains what it issued (copies, MMAs, stores)
+// and frees its tensor memory, and the first element of its first tile is set
+// to NaN.
 #pragma once
 
 #include <cuda.h>
@@ -37,21 +50,30 @@
 namespace fos {
 namespace mma {
 
-constexpr int BM = 128, BN = 128;  // output tile
+constexpr int BM = 128, BN = 256;  // output tile
 constexpr int kGroupM = 16;        // tile rows per band of the tile order
 constexpr int kKBytes = 128;       // code bytes per row per stage (256 K elements)
-constexpr int kThreadsMM = 192;
-constexpr uint32_t kTmemCols = 256;  // accumulator BN columns + scale columns
-constexpr int kABytes = BM * kKBytes, kBBytes = BN * kKBytes, kSfBytes = 4 * 512;
+constexpr int kStages = 3;
+constexpr int kSfWarps = 4;
+constexpr uint32_t kTmemCols = 512;
+constexpr int kABytes = BM * kKBytes, kBBytes = BN * kKBytes;
+constexpr int kSfBytes = 4 * 512;                 // scale atoms of a stage, 128 rows
+constexpr int kSfbBytes = (BN / 128) * kSfBytes;  // b's scale atoms of a stage
+constexpr int kSfCols = 16 + 4 * 4 * (BN / 128);  // scale columns of a stage: a 16, b 32
+constexpr int kChunkBytes = 32 * 32 * 4;          // epilogue chunk: 32 rows x 32 fp32
+static_assert(BN + 2 * kSfCols <= (int)kTmemCols, "tensor memory");
 
-template <int kStages>
+constexpr int threads_mm(int epi) { return 32 * (2 + kSfWarps + epi); }
+template <int kEpi, int kBufs>
 constexpr int smem_bytes() {
-    return kStages * (kABytes + kBBytes + 2 * kSfBytes) + 1024;  // + alignment slack
+    return kStages * (kABytes + kBBytes + kSfBytes + kSfbBytes) + kEpi * kBufs * kChunkBytes +
+           1024;  // + alignment slack
 }
 
 struct MmArgs {
     CUtensorMap ta;      // a codes [M, K/2] u8, box 128 x BM, 128-byte swizzle
     CUtensorMap tb;      // b codes [N, K/2] u8, box 128 x BN, 128-byte swizzle
+    CUtensorMap to;      // out [M, N] fp32, box 32 x 32, 128-byte swizzle
     const uint8_t* sfa;  // a scales, tiled layout
     const uint8_t* sfb;  // b scales, tiled layout
     const float* a_amax;
@@ -64,25 +86,19 @@ struct MmArgs {
     float six_bound;
 };
 
-template <int kStages>
 struct __align__(8) MmShared {
-    uint64_t full[kStages], empty[kStages], done;
+    uint64_t full[kStages], empty[kStages], sf_ready[kStages], acc_full, acc_empty, mma_done;
     uint32_t tmem;
     int fail;
 };
 
-// Shared-memory matrix descriptors (tcgen05): start address >> 4 in bits
-// 0-13, leading byte offset >> 4 in 16-29, stride byte offset >> 4 in 32-45,
-// descriptor version 1 in 46-47, layout in 61-63.
-// K-major, 128-byte swizzle: rows of 128 bytes, 8-row atoms 1024 bytes apart.
+// Shared-memory matrix descriptor (tcgen05) of a K-major operand with the
+// 128-byte swizzle: start address >> 4 in bits 0-13, leading byte offset 16
+// (>> 4) in 16-29, 8-row atoms 1024 bytes apart (>> 4) in 32-45, descriptor
+// version 1 in 46-47, layout 2 (128-byte swizzle) in 61-63.
 __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
     return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) |
            ((uint64_t)(1024 >> 4) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
-}
-// No swizzle: 8-row x 16-byte core matrices 128 bytes apart (a scale atom).
-__device__ __forceinline__ uint64_t desc_atom(uint32_t saddr) {
-    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)(128 >> 4) << 16) |
-           ((uint64_t)(128 >> 4) << 32) | ((uint64_t)1 << 46);
 }
 // Instruction descriptor of kind::mxf4nvf4: A and B E2M1 (1 in bits 7-9 and
 // 10-12), K-major, dense, UE4M3 scales (bit 23 = 0), N >> 3 in bits 17-22,
@@ -93,8 +109,11 @@ constexpr uint32_t kIdesc =
 __device__ __forceinline__ void bar_init(uint64_t* b, uint32_t n) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(b)), "r"(n) : "memory");
 }
+__device__ __forceinline__ void bar_arrive(uint64_t* b) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(b)) : "memory");
+}
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
-                                                 uint64_t* bar) {
+                                          uint64_t* bar) {
     asm volatile(
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
             "r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)) : "memory");
@@ -109,39 +128,51 @@ __device__ __forceinline__ void tc_commit(uint64_t* bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::
                      "r"(smem_u32(bar)) : "memory");
 }
+__device__ __forceinline__ void tmem_st_x4(uint32_t taddr, uint4 v) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr),
+                 "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+}
 
-template <int kStages, int kMinCtas>
-__global__ void __launch_bounds__(kThreadsMM, kMinCtas) k_mm_nvfp4(const __grid_constant__ MmArgs a) {
+// Tile order: bands of kGroupM tile rows; inside a band the tiles run down
+// the rows first, so the tiles in flight at one time cover a compact block
+// of out whose a and b tiles stay in L2.
+__device__ __forceinline__ void tile_coords(const MmArgs& a, int64_t t, int64_t& m0, int64_t& n0) {
+    const int64_t band = t / (kGroupM * a.tiles_n);
+    const int64_t rows_in_band = min((int64_t)kGroupM, a.tiles_m - band * kGroupM);
+    const int64_t r = t - band * kGroupM * a.tiles_n;
+    m0 = (band * kGroupM + r % rows_in_band) * BM;
+    n0 = (r / rows_in_band) * BN;
+}
+
+// kEpi epilogue warps (4 or 8), kBufs staging chunks per epilogue warp.
+template <int kEpi, int kBufs>
+__global__ void __launch_bounds__(threads_mm(kEpi), 1) k_mm_nvfp4(const __grid_constant__ MmArgs a) {
+    static_assert(kEpi == 4 || kEpi == 8, "epilogue warps");
+    static_assert(kBufs >= 1 && kBufs <= 3, "staging chunks");
     chain_wait();
     chain_release();
     extern __shared__ __align__(1024) unsigned char s_raw[];
-    __shared__ MmShared<kStages> sh;
+    __shared__ MmShared sh;
     // TMA swizzle atoms need 1024-byte aligned stages: round the base up
     unsigned char* sA = s_raw + ((1024u - (smem_u32(s_raw) & 1023u)) & 1023u);
     unsigned char* sB = sA + kStages * kABytes;
     unsigned char* sSA = sB + kStages * kBBytes;
     unsigned char* sSB = sSA + kStages * kSfBytes;
+    unsigned char* sOut = sSB + kStages * kSfbBytes;  // 1024-aligned chunks
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // Tile order: bands of kGroupM tile rows; inside a band the tiles run
-    // down the rows first, so the CTAs resident at one time cover a compact
-    // block of out (about 16 x 19 tiles) whose a and b tiles stay in L2.
-    int64_t m0, n0;
-    {
-        const int64_t t = blockIdx.x;
-        const int64_t band = t / (kGroupM * a.tiles_n);
-        const int64_t rows_in_band = min((int64_t)kGroupM, a.tiles_m - band * kGroupM);
-        const int64_t r = t - band * kGroupM * a.tiles_n;
-        m0 = (band * kGroupM + r % rows_in_band) * BM;
-        n0 = (r / rows_in_band) * BN;
-    }
     const int kb64 = (int)(a.K / 64);  // MMA K steps
     const int nkb = (kb64 + 3) / 4;    // stages of up to four steps
+    const int64_t tiles = a.tiles_m * a.tiles_n;
+    const int64_t sf_tiles_n = (a.N + 127) / 128;  // 128-row scale tiles of b
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             bar_init(&sh.full[s], 1);
             bar_init(&sh.empty[s], 1);
+            bar_init(&sh.sf_ready[s], kSfWarps);
         }
-        bar_init(&sh.done, 1);
+        bar_init(&sh.acc_full, 1);
+        bar_init(&sh.acc_empty, kEpi);
+        bar_init(&sh.mma_done, 1);
         sh.fail = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -154,110 +185,212 @@ __global__ void __launch_bounds__(kThreadsMM, kMinCtas) k_mm_nvfp4(const __grid_
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = sh.tmem;
-    if (warp == 0 && lane == 0) {
-        uint32_t issued[kStages] = {};  // uses of each stage issued
-        for (int i = 0; i < nkb; ++i) {
-            const int s = i % kStages;
-            if (i >= kStages && !mbar_wait(&sh.empty[s], ((i / kStages) - 1) & 1)) {
-                sh.fail = 1;
-                break;
-            }
-            const int nk = min(4, kb64 - 4 * i);
-            mbar_expect_tx(&sh.full[s], (uint32_t)(kABytes + kBBytes + 2 * nk * 512));
-            tma_load_2d(sA + s * kABytes, &a.ta, i * kKBytes, (int32_t)m0, &sh.full[s]);
-            tma_load_2d(sB + s * kBBytes, &a.tb, i * kKBytes, (int32_t)n0, &sh.full[s]);
-            bulk_load(sSA + s * kSfBytes, a.sfa + ((m0 / 128) * kb64 + 4 * i) * 512,
-                             (uint32_t)(nk * 512), &sh.full[s]);
-            bulk_load(sSB + s * kSfBytes, a.sfb + ((n0 / 128) * kb64 + 4 * i) * 512,
-                             (uint32_t)(nk * 512), &sh.full[s]);
-            issued[s] = (uint32_t)(i / kStages + 1);
-        }
-        // every copy issued has landed before the CTA can leave
-        for (int s = 0; s < kStages; ++s)
-            if (issued[s] && !mbar_wait(&sh.full[s], (issued[s] - 1) & 1)) sh.fail = 1;
-    } else if (warp == 1 && lane == 0) {
-        for (int i = 0; i < nkb; ++i) {
-            const int s = i % kStages;
-            if (!mbar_wait(&sh.full[s], (i / kStages) & 1)) {
-                sh.fail = 1;
-                break;
-            }
-            tc_fence_after();
-            const int nk = min(4, kb64 - 4 * i);
-            // scale columns of this stage: a at +0, b at +16 (four steps of
-            // four columns); alternate halves so a stage never overwrites
-            // scales the previous stage's MMAs may still read
-            const uint32_t sfc = tmem + BN + (uint32_t)((i & 1) * 32);
-            for (int kk = 0; kk < nk; ++kk) {
-                asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(sfc + kk * 4),
-                             "l"(desc_atom(smem_u32(sSA + s * kSfBytes + kk * 512))) : "memory");
-                asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(sfc + 16 + kk * 4),
-                             "l"(desc_atom(smem_u32(sSB + s * kSfBytes + kk * 512))) : "memory");
-            }
-            const uint32_t a0 = smem_u32(sA + s * kABytes), b0 = smem_u32(sB + s * kBBytes);
-            for (int kk = 0; kk < nk; ++kk) {
-                // K step kk: 32 bytes into each 128-byte swizzled row
-                const uint64_t ad = desc_sw128(a0 + kk * 32), bd = desc_sw128(b0 + kk * 32);
-                const uint32_t accumulate = (i > 0 || kk > 0) ? 1u : 0u;
-                asm volatile(
-                    "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
-                    "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, "
-                    "%3, [%4], [%5], p;\n\t}" ::"r"(tmem),
-                    "l"(ad), "l"(bd), "r"(kIdesc), "r"(sfc + kk * 4), "r"(sfc + 16 + kk * 4),
-                    "r"(accumulate)
-                    : "memory");
-            }
-            tc_commit(&sh.empty[s]);
-        }
-        tc_commit(&sh.done);  // arrives once every MMA issued above has completed
-    } else if (warp >= 2) {
-        const int q = warp & 3;  // tensor-memory lanes 32 q .. 32 q + 31
-        const bool ok = mbar_wait(&sh.done, 0);
-        __syncwarp();
-        tc_fence_after();
-        const int64_t m = m0 + 32 * q + lane;
-        const float gb = fdiv(1.0f, global_scale(a.b_amax[0], a.six_bound));
-        float ga = 0.0f;
-        if (m < a.M) ga = fdiv(1.0f, global_scale(a.a_amax[a.a_row ? m : 0], a.six_bound));
-        for (int c0 = 0; c0 < BN; c0 += 32) {
-            uint32_t v[32];
-            const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)c0;
-            asm volatile(
-                "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
-                "%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-                : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
-                  "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]),
-                  "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]),
-                  "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]),
-                  "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]),
-                  "=r"(v[31])
-                : "r"(taddr));
-            asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-            const int64_t n = n0 + c0;
-            if (m < a.M && n < a.N) {
-                float* dst = a.out + m * a.N + n;
-#pragma unroll
-                for (int j = 0; j < 32; j += 4) {
-                    if (n + j < a.N) {  // N % 16 == 0: four columns are all in or all out
-                        float4 o;
-                        o.x = fmul(fmul(__uint_as_float(v[j]), ga), gb);
-                        o.y = fmul(fmul(__uint_as_float(v[j + 1]), ga), gb);
-                        o.z = fmul(fmul(__uint_as_float(v[j + 2]), ga), gb);
-                        o.w = fmul(fmul(__uint_as_float(v[j + 3]), ga), gb);
-                        // streamed (evict-first): out must not push the
-                        // operand tiles out of L2
-                        asm volatile("st.global.cs.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst + j),
-                                     "f"(o.x), "f"(o.y), "f"(o.z), "f"(o.w) : "memory");
+    if (warp == 0) {
+        if (lane == 0) {
+            uint32_t g = 0;  // stages issued so far, over all tiles
+            bool bad = false;
+            for (int64_t t = blockIdx.x; t < tiles && !bad; t += gridDim.x) {
+                int64_t m0, n0;
+                tile_coords(a, t, m0, n0);
+                const bool b1 = n0 / 128 + 1 < sf_tiles_n;  // b's second 128 rows exist
+                for (int i = 0; i < nkb; ++i, ++g) {
+                    const int s = (int)(g % kStages);
+                    if (g >= (uint32_t)kStages &&
+                        !mbar_wait(&sh.empty[s], ((g / kStages) - 1) & 1)) {
+                        bad = true;
+                        break;
                     }
+                    const int nk = min(4, kb64 - 4 * i);
+                    mbar_expect_tx(&sh.full[s],
+                                   (uint32_t)(kABytes + kBBytes + (b1 ? 3 : 2) * nk * 512));
+                    tma_load_2d(sA + s * kABytes, &a.ta, i * kKBytes, (int32_t)m0, &sh.full[s]);
+                    tma_load_2d(sB + s * kBBytes, &a.tb, i * kKBytes, (int32_t)n0, &sh.full[s]);
+                    bulk_load(sSA + s * kSfBytes, a.sfa + ((m0 / 128) * kb64 + 4 * i) * 512,
+                              (uint32_t)(nk * 512), &sh.full[s]);
+                    bulk_load(sSB + s * kSfbBytes, a.sfb + ((n0 / 128) * kb64 + 4 * i) * 512,
+                              (uint32_t)(nk * 512), &sh.full[s]);
+                    if (b1)
+                        bulk_load(sSB + s * kSfbBytes + kSfBytes,
+                                  a.sfb + ((n0 / 128 + 1) * kb64 + 4 * i) * 512,
+                                  (uint32_t)(nk * 512), &sh.full[s]);
+                }
+            }
+            if (bad) sh.fail = 1;
+            // every copy issued has landed before the CTA can leave
+            for (uint32_t s = 0; s < (uint32_t)kStages; ++s)
+                if (g > s && !mbar_wait(&sh.full[s], ((g - 1 - s) / kStages) & 1)) sh.fail = 1;
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            uint32_t g = 0;
+            bool bad = false;
+            int j = 0;
+            for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x, ++j) {
+                // the epilogue has read the previous tile's accumulator
+                if (j > 0 && !mbar_wait(&sh.acc_empty, (j - 1) & 1)) {
+                    bad = true;
+                    break;
+                }
+                tc_fence_after();
+                for (int i = 0; i < nkb; ++i, ++g) {
+                    const int s = (int)(g % kStages);
+                    if (!mbar_wait(&sh.full[s], (g / kStages) & 1) ||
+                        !mbar_wait(&sh.sf_ready[s], (g / kStages) & 1)) {
+                        bad = true;
+                        break;
+                    }
+                    tc_fence_after();
+                    const int nk = min(4, kb64 - 4 * i);
+                    // scales of this stage: a at +0 (4 columns per K step),
+                    // b at +16 (8 per K step: 4 per 128 rows)
+                    const uint32_t sfc = tmem + (uint32_t)(BN + (g & 1) * kSfCols);
+                    const uint32_t a0 = smem_u32(sA + s * kABytes), b0 = smem_u32(sB + s * kBBytes);
+                    for (int kk = 0; kk < nk; ++kk) {
+                        // K step kk: 32 bytes into each 128-byte swizzled row
+                        const uint64_t ad = desc_sw128(a0 + kk * 32), bd = desc_sw128(b0 + kk * 32);
+                        const uint32_t accumulate = (i > 0 || kk > 0) ? 1u : 0u;
+                        asm volatile(
+                            "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+                            "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X "
+                            "[%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(tmem),
+                            "l"(ad), "l"(bd), "r"(kIdesc), "r"(sfc + kk * 4),
+                            "r"(sfc + 16 + kk * 8), "r"(accumulate)
+                            : "memory");
+                    }
+                    tc_commit(&sh.empty[s]);
+                }
+                if (bad) break;
+                tc_commit(&sh.acc_full);
+            }
+            if (bad) sh.fail = 1;
+            // every MMA issued has completed before the tensor memory is freed
+            tc_commit(&sh.mma_done);
+            if (!mbar_wait(&sh.mma_done, 0)) sh.fail = 1;
+        }
+    } else if (warp < 2 + kSfWarps) {
+        // scale warps: warp w writes tensor-memory lanes 32 q .. 32 q + 31,
+        // q = w % 4; lane j takes 16-byte row j of each atom (four columns)
+        const int q = warp & 3;
+        uint32_t g = 0;
+        bool bad = false;
+        for (int64_t t = blockIdx.x; t < tiles && !bad; t += gridDim.x) {
+            int64_t m0, n0;
+            tile_coords(a, t, m0, n0);
+            const bool b1 = n0 / 128 + 1 < sf_tiles_n;
+            for (int i = 0; i < nkb; ++i, ++g) {
+                const int s = (int)(g % kStages);
+                // the stage's atoms have landed, and scale buffer g & 1 was
+                // last read by the MMAs of stage g - 2, which have completed
+                if (!mbar_wait(&sh.full[s], (g / kStages) & 1) ||
+                    (g >= 2 && !mbar_wait(&sh.empty[(g - 2) % kStages], ((g - 2) / kStages) & 1))) {
+                    bad = true;
+                    break;
+                }
+                tc_fence_after();
+                const int nk = min(4, kb64 - 4 * i);
+                const uint32_t sfc =
+                    tmem + (uint32_t)(BN + (g & 1) * kSfCols) + ((uint32_t)(32 * q) << 16);
+                const unsigned char* pa = sSA + s * kSfBytes + 16 * lane;
+                const unsigned char* pb = sSB + s * kSfbBytes + 16 * lane;
+                for (int kk = 0; kk < nk; ++kk) {
+                    tmem_st_x4(sfc + 4 * kk, *reinterpret_cast<const uint4*>(pa + kk * 512));
+                    tmem_st_x4(sfc + 16 + 8 * kk, *reinterpret_cast<const uint4*>(pb + kk * 512));
+                    if (b1)
+                        tmem_st_x4(sfc + 16 + 8 * kk + 4,
+                                   *reinterpret_cast<const uint4*>(pb + kSfBytes + kk * 512));
+                }
+                asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) bar_arrive(&sh.sf_ready[s]);
+            }
+        }
+        if (bad) sh.fail = 1;
+    } else {
+        // epilogue: warp e reads lanes 32 q .. of columns [c_beg, c_beg + kCols)
+        const int q = warp & 3;
+        const int e = warp - 2 - kSfWarps;
+        constexpr int kCols = BN / (kEpi / 4);
+        const int c_beg = (e / 4) * kCols;
+        const float gb = fdiv(1.0f, global_scale(a.b_amax[0], a.six_bound));
+        const float ga0 = a.a_row ? 0.0f : fdiv(1.0f, global_scale(a.a_amax[0], a.six_bound));
+        int j = 0, chunk = 0;
+        for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x, ++j) {
+            if (!mbar_wait(&sh.acc_full, j & 1)) {
+                sh.fail = 1;
+                break;
+            }
+            __syncwarp();
+            tc_fence_after();
+            int64_t m0, n0;
+            tile_coords(a, t, m0, n0);
+            const int64_t m = m0 + 32 * q + lane;
+            float ga = ga0;
+            if (a.a_row && m < a.M) ga = fdiv(1.0f, global_scale(a.a_amax[m], a.six_bound));
+            for (int c0 = c_beg; c0 < c_beg + kCols; c0 += 32, ++chunk) {
+                uint32_t v[32];
+                const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)c0;
+                asm volatile(
+                    "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,"
+                    "%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,"
+                    "%30,%31}, [%32];"
+                    : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]),
+                      "=r"(v[6]), "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]),
+                      "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]),
+                      "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]),
+                      "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]), "=r"(v[26]),
+                      "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+                    : "r"(taddr));
+                asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+                if (c0 + 32 == c_beg + kCols) {  // this warp's columns read: the MMA may go on
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) bar_arrive(&sh.acc_empty);
+                }
+                // staging chunk of this warp: the store issued kBufs chunks
+                // ago must have finished reading it
+                unsigned char* buf = sOut + (e * kBufs + chunk % kBufs) * kChunkBytes;
+                if (lane == 0) {
+                    if constexpr (kBufs == 1)
+                        asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+                    else if constexpr (kBufs == 2)
+                        asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+                    else
+                        asm volatile("cp.async.bulk.wait_group.read 2;" ::: "memory");
+                }
+                __syncwarp();
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {  // 16-byte piece k of row `lane`, 128-byte swizzle
+                    const uint32_t addr = smem_u32(buf) + lane * 128 + ((k ^ (lane & 7)) * 16);
+                    asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr),
+                                 "f"(fmul(fmul(__uint_as_float(v[4 * k]), ga), gb)),
+                                 "f"(fmul(fmul(__uint_as_float(v[4 * k + 1]), ga), gb)),
+                                 "f"(fmul(fmul(__uint_as_float(v[4 * k + 2]), ga), gb)),
+                                 "f"(fmul(fmul(__uint_as_float(v[4 * k + 3]), ga), gb))
+                                 : "memory");
+                }
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) {
+                    asm volatile(
+                        "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], "
+                        "[%3];" ::"l"(&a.to),
+                        "r"((int32_t)(n0 + c0)), "r"((int32_t)(m0 + 32 * q)), "r"(smem_u32(buf))
+                        : "memory");
+                    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
                 }
             }
         }
-        if (!ok) sh.fail = 1;
+        if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+        __syncwarp();
     }
     tc_fence_before();
     __syncthreads();
-    if (sh.fail && threadIdx.x == 0 && m0 < a.M && n0 < a.N)
+    if (sh.fail && threadIdx.x == 0 && (int64_t)blockIdx.x < tiles) {
+        int64_t m0, n0;
+        tile_coords(a, blockIdx.x, m0, n0);
         a.out[m0 * a.N + n0] = __int_as_float(0x7FC00000);
+    }
     if (warp == 1) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),

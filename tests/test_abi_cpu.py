@@ -70,6 +70,9 @@ FAKE = ctypes.c_void_p(0x10000)  # never dereferenced: every call below fails va
     (dict(e4m3_bound=300), fos.FOS_ERR_UNSUPPORTED),
     (dict(err_order=2), fos.FOS_ERR_INVALID_ARG),
     (dict(block=1, err_order=1), fos.FOS_ERR_UNSUPPORTED),  # sequential order: 1x16 only
+    (dict(scale_layout=2), fos.FOS_ERR_INVALID_ARG),
+    (dict(scale_layout=-1), fos.FOS_ERR_INVALID_ARG),
+    (dict(block=1, scale_layout=1), fos.FOS_ERR_UNSUPPORTED),  # tiled scales: 1x16 only
 ])
 def test_quantize_rejects_bad_config(L, kw, rc):
     c = _cfg(**kw)
@@ -142,6 +145,28 @@ def test_dequantize_and_amax_and_diag_reject(L):
     assert L.fos_amax(FAKE, 0, 16, 17, 0, FAKE, None) == fos.FOS_ERR_UNSUPPORTED
     assert L.fos_diag_convert(99, FAKE, FAKE, 4, None) == fos.FOS_ERR_INVALID_ARG
     assert L.fos_diag_convert(0, FAKE, FAKE, 0, None) == fos.FOS_OK
+
+
+def test_tiled_scales_only_where_the_quantize_writes_them(L):
+    """The tiled layout is an output option of the 1x16 quantize calls; the
+    grouped quantize and the dequantize take plain scales and refuse it on
+    the host."""
+    c = _cfg(scale_layout=1)
+    assert L.fos_quantize_grouped(FAKE, 0, 32, 32, FAKE, 1, ctypes.byref(c), FAKE, FAKE, FAKE,
+                                  None) == fos.FOS_ERR_UNSUPPORTED
+    assert L.fos_dequantize(FAKE, FAKE, FAKE, 32, 32, ctypes.byref(c), FAKE, 0,
+                            None) == fos.FOS_ERR_UNSUPPORTED
+    c16 = _cfg(block=1, scale_layout=1)
+    P = ctypes.c_void_p * 1
+    rows, cols = (ctypes.c_int64 * 1)(32), (ctypes.c_int64 * 1)(32)
+    assert L.fos_quantize_list(1, P(FAKE), 0, rows, cols, ctypes.byref(c16), P(FAKE), P(FAKE),
+                               P(FAKE), None) == fos.FOS_ERR_UNSUPPORTED
+    # block positions are 32-bit: tiled scales for fewer than 2^30 rows
+    c = _cfg(scale_layout=1)
+    assert L.fos_quantize(FAKE, 0, 1 << 30, 16, ctypes.byref(c), FAKE, FAKE, FAKE,
+                          None) == fos.FOS_ERR_UNSUPPORTED
+    assert fos.Config(scale_tiled=True).c(True).scale_layout == 1
+    assert fos.Config().c(True).scale_layout == 0
 
 
 def test_python_binding_refuses_cpu_tensors():

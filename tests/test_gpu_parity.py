@@ -882,11 +882,11 @@ def _at16(t):
 
 
 def test_mm_in_row_chunks_with_16_byte_aligned_operands():
-    """A product whose fp32 output is larger than half the L2 runs as several
-    row-chunk GEMMs, each followed by its epilogue; operands and output
-    placed 16 bytes into their buffers.  Sampled rows of every chunk (and the
-    ragged last one), row-scaled a, against the oracle's block values within
-    the fp32 accumulation bound."""
+    """A wide product (17 x 64 output tiles, more than one per SM, so each
+    CTA of the persistent kernel walks several and its accumulator is
+    reused); operands and output placed 16 bytes into their buffers.  Sampled
+    rows of every 768-row band, row-scaled a, against the oracle's block
+    values within the fp32 accumulation bound."""
     M, N, K = 2176, 16384, 128
     gcfg_a, ocfg_a = _cfgs("mse", 448, True)
     gcfg_b, ocfg_b = _cfgs("mse", 448)
