@@ -4,38 +4,45 @@
 // in the epilogue (grouped PR, the dense-recipe commit's four_over_six_mm
 // forward; per row of a for a row-scaled a, the MoE commit's epilogue).
 //
-// A persistent kernel: one CTA per SM walks BM x BN = 128 x 256 output tiles
-// (tile t, t + grid, ...).  Warp roles:
+// A persistent kernel: one CTA per SM walks BM x BN = 128 x 192 output tiles
+// (tile t, t + grid, ...), with two accumulators in tensor memory so that
+// the epilogue of one tile runs while the MMAs of the next fill the other.
+// Warp roles:
 //   warp 0      (one thread) TMA producer: per K stage of 256 elements, the a
 //               and b code tiles (2D TMA, 128-byte swizzle) and the stage's
-//               512-byte scale atoms (1D bulk copies: four for a, four per
-//               128 rows of b) into a ring of kStages shared-memory stages;
+//               512-byte scale atoms (1D bulk copies: four for a, four for
+//               each of the two 128-row scale tiles b's 192 rows touch) into
+//               a ring of kStages shared-memory stages;
 //   warp 1      allocates the tensor memory; one thread issues per stage four
 //               tcgen05.mma kind::mxf4nvf4 block_scale scale_vec::4X
-//               (M = 128, N = 256, K = 64 each) into the accumulator, then
-//               frees the stage (tcgen05.commit to its mbarrier) and, after a
-//               tile's last stage, hands the accumulator to the epilogue;
+//               (M = 128, N = 192, K = 64 each) into the tile's accumulator,
+//               then frees the stage (tcgen05.commit to its mbarrier) and,
+//               after a tile's last stage, hands the accumulator to the
+//               epilogue;
 //   warps 2-5   scale warps: move each stage's scale atoms from shared to
-//               tensor memory (ld.shared + tcgen05.st), warp w into the lanes
-//               32 (w % 4) .. 32 (w % 4) + 31 it may write;
+//               tensor memory (ld.shared, two tcgen05.st of 16 and 32
+//               columns), warp w into the lanes 32 (w % 4) .. 32 (w % 4) + 31
+//               it may write;
 //   warps 6-..  epilogue (kEpi warps, kEpi / 4 per lane quadrant): read the
 //               FP32 accumulator (tcgen05.ld), multiply by g_a(m) and then
 //               g_b, stage 32 x 32 chunks in shared memory in the 128-byte
 //               swizzle and store them with TMA (cp.async.bulk.tensor), which
 //               clips the rows and columns past the end of out.
-// The accumulator (256 columns) and two scale buffers (48 columns each: a
-// stage's scales are written while the previous stage's MMAs read theirs)
-// take 352 of the 512 tensor-memory columns.
+// Two accumulators (192 columns each) and two scale buffers (48 columns
+// each: a stage's scales are written while the previous stage's MMAs read
+// theirs) take 480 of the 512 tensor-memory columns.
 //
 // Operands are K-major: a row of a (or b) holds K/2 code bytes, element 2j in
 // the low nibble of byte j, which is the element order of the E2M1 operand.
 // The scale atom of rows [128 t, 128 t + 128) and K elements [64 c, 64 c + 64)
 // is the 512-byte tile (t, c) of the tiled layout: byte 16 j + 4 i + k holds
-// the scale of row 32 i + j, 16-element block k.  The MMA reads the scales of
-// row r (of a, or of the 128-row half h of b) from tensor-memory lane
-// 32 q + r % 32, column c0 + r / 32 (+ 4 h for b), for each quadrant q: a
-// scale warp of quadrant q stores 16-byte row j of the atom (columns c0 ..
-// c0 + 3) to its lane 32 q + j, which is that content.
+// the scale of row 32 i + j, 16-element block k.  The MMA reads the four
+// scales of row r of its a (b) tile from tensor-memory lane 32 q + r % 32,
+// column c0 + r / 32, for each quadrant q: a scale warp of quadrant q stores
+// word i of 16-byte row j of the atom to its lane 32 q + j, column c0 + i.
+// A b tile starts at n0 = 192 t, at row 0 or row 64 of a scale tile: its
+// six 32-row groups are words 0-3 of the first atom and 0-1 of the next, or
+// words 2-3 of the first and 0-3 of the next.
 //
 // Every mbarrier wait is bounded (about a second); a wait that gives up marks
 // the CTA failed, the CTA still drains what it issued (copies, MMAs, stores)
@@ -50,18 +57,19 @@
 namespace fos {
 namespace mma {
 
-constexpr int BM = 128, BN = 256;  // output tile
+constexpr int BM = 128, BN = 192;  // output tile
 constexpr int kGroupM = 16;        // tile rows per band of the tile order
 constexpr int kKBytes = 128;       // code bytes per row per stage (256 K elements)
-constexpr int kStages = 3;
+constexpr int kStages = 4;
 constexpr int kSfWarps = 4;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kABytes = BM * kKBytes, kBBytes = BN * kKBytes;
 constexpr int kSfBytes = 4 * 512;                 // scale atoms of a stage, 128 rows
-constexpr int kSfbBytes = (BN / 128) * kSfBytes;  // b's scale atoms of a stage
-constexpr int kSfCols = 16 + 4 * 4 * (BN / 128);  // scale columns of a stage: a 16, b 32
+constexpr int kSfbBytes = 2 * kSfBytes;           // b's scale atoms of a stage (two tiles)
+constexpr int kSfCols = 16 + 32;                  // scale columns of a stage: a 4, b 8 per K step
 constexpr int kChunkBytes = 32 * 32 * 4;          // epilogue chunk: 32 rows x 32 fp32
-static_assert(BN + 2 * kSfCols <= (int)kTmemCols, "tensor memory");
+constexpr int kAccCols = 2 * BN;                  // two accumulators
+static_assert(kAccCols + 2 * kSfCols <= (int)kTmemCols, "tensor memory");
 
 constexpr int threads_mm(int epi) { return 32 * (2 + kSfWarps + epi); }
 template <int kEpi, int kBufs>
@@ -87,7 +95,7 @@ struct MmArgs {
 };
 
 struct __align__(8) MmShared {
-    uint64_t full[kStages], empty[kStages], sf_ready[kStages], acc_full, acc_empty, mma_done;
+    uint64_t full[kStages], empty[kStages], sf_ready[kStages], acc_full[2], acc_empty[2], mma_done;
     uint32_t tmem;
     int fail;
 };
@@ -128,9 +136,27 @@ __device__ __forceinline__ void tc_commit(uint64_t* bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::
                      "r"(smem_u32(bar)) : "memory");
 }
-__device__ __forceinline__ void tmem_st_x4(uint32_t taddr, uint4 v) {
-    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr),
-                 "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+// tcgen05.st of 16 and 32 consecutive columns (32x32b shape: register c of
+// lane l goes to lane 32 q + l, column taddr + c).
+__device__ __forceinline__ void tmem_st_x16(uint32_t taddr, const uint32_t (&v)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+        "%13,%14,%15,%16};" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+        "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+        : "memory");
+}
+__device__ __forceinline__ void tmem_st_x32(uint32_t taddr, const uint32_t (&v)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+        "%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(
+            taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+        "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]),
+        "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]),
+        "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]),
+        "r"(v[30]), "r"(v[31])
+        : "memory");
 }
 
 // Tile order: bands of kGroupM tile rows; inside a band the tiles run down
@@ -170,8 +196,10 @@ __global__ void __launch_bounds__(threads_mm(kEpi), 1) k_mm_nvfp4(const __grid_c
             bar_init(&sh.empty[s], 1);
             bar_init(&sh.sf_ready[s], kSfWarps);
         }
-        bar_init(&sh.acc_full, 1);
-        bar_init(&sh.acc_empty, kEpi);
+        for (int b = 0; b < 2; ++b) {
+            bar_init(&sh.acc_full[b], 1);
+            bar_init(&sh.acc_empty[b], kEpi);
+        }
         bar_init(&sh.mma_done, 1);
         sh.fail = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -192,7 +220,7 @@ __global__ void __launch_bounds__(threads_mm(kEpi), 1) k_mm_nvfp4(const __grid_c
             for (int64_t t = blockIdx.x; t < tiles && !bad; t += gridDim.x) {
                 int64_t m0, n0;
                 tile_coords(a, t, m0, n0);
-                const bool b1 = n0 / 128 + 1 < sf_tiles_n;  // b's second 128 rows exist
+                const bool b1 = n0 / 128 + 1 < sf_tiles_n;  // b's second scale tile exists
                 for (int i = 0; i < nkb; ++i, ++g) {
                     const int s = (int)(g % kStages);
                     if (g >= (uint32_t)kStages &&
@@ -226,12 +254,14 @@ __global__ void __launch_bounds__(threads_mm(kEpi), 1) k_mm_nvfp4(const __grid_c
             bool bad = false;
             int j = 0;
             for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x, ++j) {
-                // the epilogue has read the previous tile's accumulator
-                if (j > 0 && !mbar_wait(&sh.acc_empty, (j - 1) & 1)) {
+                // the epilogue has read this accumulator's previous tile
+                const int ab = j & 1;
+                if (j >= 2 && !mbar_wait(&sh.acc_empty[ab], ((j >> 1) - 1) & 1)) {
                     bad = true;
                     break;
                 }
                 tc_fence_after();
+                const uint32_t acc = tmem + (uint32_t)(ab * BN);
                 for (int i = 0; i < nkb; ++i, ++g) {
                     const int s = (int)(g % kStages);
                     if (!mbar_wait(&sh.full[s], (g / kStages) & 1) ||
@@ -243,7 +273,7 @@ __global__ void __launch_bounds__(threads_mm(kEpi), 1) k_mm_nvfp4(const __grid_c
                     const int nk = min(4, kb64 - 4 * i);
                     // scales of this stage: a at +0 (4 columns per K step),
                     // b at +16 (8 per K step: 4 per 128 rows)
-                    const uint32_t sfc = tmem + (uint32_t)(BN + (g & 1) * kSfCols);
+                    const uint32_t sfc = tmem + (uint32_t)(kAccCols + (g & 1) * kSfCols);
                     const uint32_t a0 = smem_u32(sA + s * kABytes), b0 = smem_u32(sB + s * kBBytes);
                     for (int kk = 0; kk < nk; ++kk) {
                         // K step kk: 32 bytes into each 128-byte swizzled row
@@ -252,7 +282,7 @@ __global__ void __launch_bounds__(threads_mm(kEpi), 1) k_mm_nvfp4(const __grid_c
                         asm volatile(
                             "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
                             "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X "
-                            "[%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(tmem),
+                            "[%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(acc),
                             "l"(ad), "l"(bd), "r"(kIdesc), "r"(sfc + kk * 4),
                             "r"(sfc + 16 + kk * 8), "r"(accumulate)
                             : "memory");
@@ -260,7 +290,7 @@ __global__ void __launch_bounds__(threads_mm(kEpi), 1) k_mm_nvfp4(const __grid_c
                     tc_commit(&sh.empty[s]);
                 }
                 if (bad) break;
-                tc_commit(&sh.acc_full);
+                tc_commit(&sh.acc_full[ab]);
             }
             if (bad) sh.fail = 1;
             // every MMA issued has completed before the tensor memory is freed
@@ -269,7 +299,10 @@ __global__ void __launch_bounds__(threads_mm(kEpi), 1) k_mm_nvfp4(const __grid_c
         }
     } else if (warp < 2 + kSfWarps) {
         // scale warps: warp w writes tensor-memory lanes 32 q .. 32 q + 31,
-        // q = w % 4; lane j takes 16-byte row j of each atom (four columns)
+        // q = w % 4; lane j takes 16-byte row j of each atom: a's four words
+        // to columns +4 kk .. +4 kk + 3, b's six 32-row groups to columns
+        // +16 + 8 kk .. (two more columns of zeros keep each K step's b
+        // scales 8 columns apart)
         const int q = warp & 3;
         uint32_t g = 0;
         bool bad = false;
@@ -277,28 +310,39 @@ __global__ void __launch_bounds__(threads_mm(kEpi), 1) k_mm_nvfp4(const __grid_c
             int64_t m0, n0;
             tile_coords(a, t, m0, n0);
             const bool b1 = n0 / 128 + 1 < sf_tiles_n;
+            const bool off2 = (n0 & 127) != 0;  // b's rows start half-way into a scale tile
             for (int i = 0; i < nkb; ++i, ++g) {
                 const int s = (int)(g % kStages);
-                // the stage's atoms have landed, and scale buffer g & 1 was
-                // last read by the MMAs of stage g - 2, which have completed
                 if (!mbar_wait(&sh.full[s], (g / kStages) & 1) ||
                     (g >= 2 && !mbar_wait(&sh.empty[(g - 2) % kStages], ((g - 2) / kStages) & 1))) {
                     bad = true;
                     break;
                 }
                 tc_fence_after();
-                const int nk = min(4, kb64 - 4 * i);
                 const uint32_t sfc =
-                    tmem + (uint32_t)(BN + (g & 1) * kSfCols) + ((uint32_t)(32 * q) << 16);
+                    tmem + (uint32_t)(kAccCols + (g & 1) * kSfCols) + ((uint32_t)(32 * q) << 16);
                 const unsigned char* pa = sSA + s * kSfBytes + 16 * lane;
                 const unsigned char* pb = sSB + s * kSfbBytes + 16 * lane;
-                for (int kk = 0; kk < nk; ++kk) {
-                    tmem_st_x4(sfc + 4 * kk, *reinterpret_cast<const uint4*>(pa + kk * 512));
-                    tmem_st_x4(sfc + 16 + 8 * kk, *reinterpret_cast<const uint4*>(pb + kk * 512));
-                    if (b1)
-                        tmem_st_x4(sfc + 16 + 8 * kk + 4,
-                                   *reinterpret_cast<const uint4*>(pb + kSfBytes + kk * 512));
+                uint32_t va[16], vb[32];
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    const uint4 x = *reinterpret_cast<const uint4*>(pa + kk * 512);
+                    va[4 * kk] = x.x; va[4 * kk + 1] = x.y; va[4 * kk + 2] = x.z; va[4 * kk + 3] = x.w;
+                    const uint4 u0 = *reinterpret_cast<const uint4*>(pb + kk * 512);
+                    uint4 u1 = make_uint4(0, 0, 0, 0);
+                    if (b1) u1 = *reinterpret_cast<const uint4*>(pb + kSfBytes + kk * 512);
+                    // column c holds row 32 c + lane of b's 192 rows
+                    vb[8 * kk + 0] = off2 ? u0.z : u0.x;
+                    vb[8 * kk + 1] = off2 ? u0.w : u0.y;
+                    vb[8 * kk + 2] = off2 ? u1.x : u0.z;
+                    vb[8 * kk + 3] = off2 ? u1.y : u0.w;
+                    vb[8 * kk + 4] = off2 ? u1.z : u1.x;
+                    vb[8 * kk + 5] = off2 ? u1.w : u1.y;
+                    vb[8 * kk + 6] = 0;
+                    vb[8 * kk + 7] = 0;
                 }
+                tmem_st_x16(sfc, va);
+                tmem_st_x32(sfc + 16, vb);
                 asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
                 tc_fence_before();
                 __syncwarp();
@@ -316,7 +360,8 @@ __global__ void __launch_bounds__(threads_mm(kEpi), 1) k_mm_nvfp4(const __grid_c
         const float ga0 = a.a_row ? 0.0f : fdiv(1.0f, global_scale(a.a_amax[0], a.six_bound));
         int j = 0, chunk = 0;
         for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x, ++j) {
-            if (!mbar_wait(&sh.acc_full, j & 1)) {
+            const int ab = j & 1;
+            if (!mbar_wait(&sh.acc_full[ab], (j >> 1) & 1)) {
                 sh.fail = 1;
                 break;
             }
@@ -329,7 +374,7 @@ __global__ void __launch_bounds__(threads_mm(kEpi), 1) k_mm_nvfp4(const __grid_c
             if (a.a_row && m < a.M) ga = fdiv(1.0f, global_scale(a.a_amax[m], a.six_bound));
             for (int c0 = c_beg; c0 < c_beg + kCols; c0 += 32, ++chunk) {
                 uint32_t v[32];
-                const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)c0;
+                const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(ab * BN + c0);
                 asm volatile(
                     "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,"
                     "%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,"
@@ -345,7 +390,7 @@ __global__ void __launch_bounds__(threads_mm(kEpi), 1) k_mm_nvfp4(const __grid_c
                 if (c0 + 32 == c_beg + kCols) {  // this warp's columns read: the MMA may go on
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) bar_arrive(&sh.acc_empty);
+                    if (lane == 0) bar_arrive(&sh.acc_empty[ab]);
                 }
                 // staging chunk of this warp: the store issued kBufs chunks
                 // ago must have finished reading it

@@ -871,6 +871,29 @@ def test_mm_of_quantized_operands(mode, row):
     assert np.all(err <= bound + 1e-30), float((err / (bound + 1e-30)).max())
 
 
+@pytest.mark.parametrize("M,N,K", [(16, 16, 64), (304, 208, 320), (128, 400, 1024),
+                                   (1040, 592, 256), (144, 1344, 2112)])
+def test_mm_tile_edges(M, N, K):
+    """Shapes that put the edges of the 128 x 192 output tiles everywhere: N
+    below one tile, b tiles starting at row 0 and row 64 of a 128-row scale
+    tile, with and without a next scale tile, ragged M, K not a multiple of
+    the 256-element stage (partial last stage), several tiles per CTA; every
+    entry against the oracle's product reference within its fp32 bound."""
+    gcfg, ocfg = _cfgs("mse", 448, False)
+    a = _x(M, K, "F3", 71, "bf16")
+    b = _x(N, K, "F2", 72, "bf16")
+    ca, sa, aa = fos.quantize(a.to(DEV), gcfg)
+    cb, sb, ab = fos.quantize(b.to(DEV), gcfg)
+    out = fos.mm(ca, fos.swizzle_scales(sa, M, K), aa, cb, fos.swizzle_scales(sb, N, K), ab, gcfg)
+    torch.cuda.synchronize()
+    oca, osa, oaa = oracle.quantize(a.float().numpy(), ocfg)
+    ocb, osb, oab = oracle.quantize(b.float().numpy(), ocfg)
+    assert np.array_equal(ca.cpu().numpy(), oca) and np.array_equal(cb.cpu().numpy(), ocb)
+    ref, bound = oracle.mm_reference(oca, osa, oaa, ocb, osb, oab, ocfg)
+    err = np.abs(out.cpu().numpy().astype(np.float64) - ref)
+    assert np.all(err <= bound + 1e-30), float((err / (bound + 1e-30)).max())
+
+
 def _at16(t):
     """A copy of t whose storage starts 16 bytes into a larger buffer: 16-byte
     but not 256-byte aligned."""
