@@ -314,6 +314,9 @@ __global__ void __launch_bounds__(kThreads, min_ctas<EM>()) k_quant1x16(const En
 // rewritten two rows later, after every thread has passed the barrier of the
 // row in between and so finished reading it.  One barrier per row (table
 // ready) with the amax given, two with the amax computed (reduction, table).
+// With the amax given, warp 0 computes the next row's global scale while the
+// table of the current row is filled (the other warps read it from shared
+// memory), and each block is widened once.
 // ------------------------------------------------------------------------
 template <In IT, Err EM, int K, bool TL = false>
 __global__ void __launch_bounds__(kThreads) k_quant1x16_rowpass(const EncArgs a) {
@@ -321,6 +324,7 @@ __global__ void __launch_bounds__(kThreads) k_quant1x16_rowpass(const EncArgs a)
     chain_release();
     __shared__ float2 s_tbl[2][128];
     __shared__ float s_red[kWarps];
+    __shared__ float s_S[2];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint64_t nz = pk(a.neg_zero, a.neg_zero);
     constexpr int64_t kBytes = (IT == In::F32) ? 64 : 32;
@@ -336,6 +340,44 @@ __global__ void __launch_bounds__(kThreads) k_quant1x16_rowpass(const EncArgs a)
     }
     uint32_t dummy[8];
     int par = 0;
+    if (a.amax_given) {
+        // The row's global scale is computed once per CTA, by warp 0 a row
+        // ahead (into s_S, double-buffered like the table), and each block is
+        // widened once: its amax comes out of the encode.
+        float S = global_scale(a.amax[row], a.six_bound);
+        for (; row < a.rows; row += gridDim.x, par ^= 1) {
+            const int64_t rown = row + gridDim.x;
+#pragma unroll
+            for (int k = 0; k < K; ++k) {
+                const int64_t j = tid + (int64_t)k * kThreads;
+                load_if<IT, kEncHint>(nxt[k], xb + (rown * a.nb + j) * kBytes,
+                                      rown < a.rows && j < a.nb);
+            }
+            fill_table_cta(s_tbl[par], S, tid);
+            if (warp == 0 && rown < a.rows) {
+                const float Sn = global_scale(a.amax[rown], a.six_bound);
+                if (lane == 0) s_S[par] = Sn;
+            }
+            __syncthreads();
+            const float Sn = s_S[par];  // read before the next barrier: rewritten two rows on
+#pragma unroll
+            for (int k = 0; k < K; ++k) {
+                const int64_t j = tid + (int64_t)k * kThreads;
+                if (j < a.nb) {
+                    uint64_t xp[8];
+                    widen<IT>(cur[k], xp);
+                    uint32_t code[2], scale;
+                    encode_block<EM, Out::NONE>(xp, S, s_tbl[par], nz, code, scale, dummy);
+                    const int64_t b = row * a.nb + j;
+                    st64(a.codes + b * 8, code[0], code[1]);
+                    st8(a.scales + scale_at<TL>(b, row, j, a.sc_pc4), scale);
+                }
+                cur[k] = nxt[k];
+            }
+            S = Sn;
+        }
+        return;
+    }
     for (; row < a.rows; row += gridDim.x, par ^= 1) {
         const int64_t rown = row + gridDim.x;
 #pragma unroll
@@ -353,18 +395,13 @@ __global__ void __launch_bounds__(kThreads) k_quant1x16_rowpass(const EncArgs a)
             bam[k] = (tid + (int64_t)k * kThreads < a.nb) ? seg_amax(xp) : 0.0f;
             m = fmaxf(m, bam[k]);
         }
-        float A;
-        if (a.amax_given) {
-            A = a.amax[row];
-        } else {
-            m = warp_max_dev(m);
-            if (lane == 0) s_red[warp] = m;
-            __syncthreads();
-            A = 0.0f;
+        m = warp_max_dev(m);
+        if (lane == 0) s_red[warp] = m;
+        __syncthreads();
+        float A = 0.0f;
 #pragma unroll
-            for (int w = 0; w < kWarps; ++w) A = fmaxf(A, s_red[w]);
-            if (tid == 0) amax_out[row] = A;
-        }
+        for (int w = 0; w < kWarps; ++w) A = fmaxf(A, s_red[w]);
+        if (tid == 0) amax_out[row] = A;
         const float S = global_scale(A, a.six_bound);
         fill_table_cta(s_tbl[par], S, tid);
         __syncthreads();
