@@ -904,7 +904,7 @@ def _at16(t):
     return v
 
 
-def test_mm_in_row_chunks_with_16_byte_aligned_operands():
+def test_mm_many_tiles_with_16_byte_aligned_operands():
     """A wide product (17 x 64 output tiles, more than one per SM, so each
     CTA of the persistent kernel walks several and its accumulator is
     reused); operands and output placed 16 bytes into their buffers.  Sampled
