@@ -256,26 +256,38 @@ __global__ void __launch_bounds__(kThreads, min_ctas<EM>()) k_quant1x16(const En
             }
         }
         if (whole_chunks && (SRC == Src::ROW || k < a.G)) {
-            // steady state: the next unit is whole and under the same scale
+            // Steady state: the next unit is whole and under the same scale.
+            // With whole chunks, unit v's block of this lane is v * 32 + lane
+            // in the flat block order, so the walk just adds 32 (the row and
+            // chunk are recovered once, when it ends).
             const int64_t seg_end = (SRC == Src::ROW) ? cc.row + 1 : (int64_t)s_ends[k];
-            while (u + 1 < u1) {
-                RowChunk nc = cc;
-                nc.next(a.cpr);
-                if (nc.row >= seg_end) break;
-                const int64_t jn = nc.chunk * 32 + lane;
-                Raw<IT> nxt;
-                load_seg<IT, kEncHint>(nxt, xb + (nc.row * a.nb + jn) * kBytes);
-                uint64_t xp[8];
-                widen<IT>(cur, xp);
-                uint32_t code[2], scale;
-                encode_block<EM, Out::NONE, SRC == Src::GROUP>(xp, S, tbl, nz, code, scale, dummy);
-                const int64_t b = cc.row * a.nb + j;
-                st64(a.codes + b * 8, code[0], code[1]);
-                st8(a.scales + scale_at<TL>(b, cc.row, j, a.sc_pc4), scale);
-                cur = nxt;
-                cc = nc;
-                j = jn;
-                ++u;
+            const int64_t u_end = min(u1, seg_end * a.cpr);  // past this warp's units of the segment
+            if (u + 1 < u_end) {
+                int64_t b = u * 32 + lane;
+                BlockPos pos;
+                if constexpr (TL) {
+                    pos.row = (int32_t)cc.row;
+                    pos.col = (int32_t)j;
+                }
+                const int32_t nb32 = (int32_t)a.nb;
+                do {
+                    Raw<IT> nxt;
+                    load_seg<IT, kEncHint>(nxt, xb + (b + 32) * kBytes);
+                    uint64_t xp[8];
+                    widen<IT>(cur, xp);
+                    uint32_t code[2], scale;
+                    encode_block<EM, Out::NONE, SRC == Src::GROUP>(xp, S, tbl, nz, code, scale,
+                                                                   dummy);
+                    st64(a.codes + b * 8, code[0], code[1]);
+                    st8(a.scales + scale_at<TL>(b, pos.row, pos.col, a.sc_pc4), scale);
+                    if constexpr (TL) pos.advance(0, 32, nb32);
+                    cur = nxt;
+                    b += 32;
+                    ++u;
+                } while (u + 1 < u_end);
+                cc.row = u / a.cpr;
+                cc.chunk = u - cc.row * a.cpr;
+                j = cc.chunk * 32 + lane;
             }
         }
         RowChunk nc = cc;
