@@ -243,19 +243,21 @@ FOS_API fos_status fos_swizzle_scales(const uint8_t* scales, int64_t rows, int64
  * fos_mm -- out = a . b^T from quantized operands, the forward product of
  * the grouped PR's four_over_six_mm: a [M, K] and b [N, K] were quantized
  * with 1x16 blocks (codes [M, K/2] and [N, K/2]) and their block scales put
- * into the tiled GEMM layout (fos_swizzle_scales); a_amax / b_amax are the
- * amaxes they were quantized with (a: [M] when cfg->granularity is
- * FOS_SCALE_ROW, else [1]; b: [1]).  One launch of this library's kernel on
- * the tensor cores (tcgen05 block-scaled E2M1 MMAs with UE4M3 scales, fp32
- * accumulation in tensor memory) forms the block-scaled product D of each
- * 128 x 128 output tile, and its epilogue applies the global decode scales
- * before the single store,
+ * into the tiled GEMM layout (fos_swizzle_scales, or written there directly
+ * by the quantize call with scale_layout = FOS_SCALES_TILED); a_amax /
+ * b_amax are the amaxes they were quantized with (a: [M] when
+ * cfg->granularity is FOS_SCALE_ROW, else [1]; b: [1]).  One persistent
+ * launch of this library's kernel on the tensor cores (tcgen05 block-scaled
+ * E2M1 MMAs with UE4M3 scales, fp32 accumulation in tensor memory, one CTA
+ * per SM walking 128 x 192 output tiles) forms the block-scaled product D
+ * of each tile, and its epilogue applies the global decode scales before
+ * the single store,
  *   out[m][n] = (D[m][n] * g_a(m)) * g_b,  g = rn(1 / S),
  * S the global scale fos_quantize used (cfg->e4m3_bound).  out: fp32
  * [M, N] row-major, 16-byte aligned, like all operands.  M and N multiples
- * of 16, K a multiple of 64.  The kernel's waits are bounded: a tile whose
- * wait gave up (which takes about a second) has NaN in its first element.
- * Nothing is allocated.
+ * of 16, K a multiple of 64.  The kernel's waits are bounded: a CTA whose
+ * wait gave up (which takes about a second) writes NaN into the first
+ * element of its first tile.  Nothing is allocated.
  */
 FOS_API fos_status fos_mm(const uint8_t* a_codes, const uint8_t* a_scales_tiled,
                           const float* a_amax, const uint8_t* b_codes,
