@@ -232,3 +232,30 @@ def test_mm_consumes_the_tiled_output_directly():
     _same(ac, _u(pac), "codes tiled vs plain")
     _same(at, _u(fos.swizzle_scales(pas, M, K)), "tiled scales vs swizzled plain")
     _same(direct, _u(via), "mm direct vs swizzled")
+
+
+def test_mm_row_scaled_from_tiled_output():
+    """A row-scaled a (the row pass, scales written tiled) times a per-tensor
+    b (list pipeline, tiled): fos_mm equals the oracle's product reference of
+    the same operands within its fp32 bound, and the tiled scales equal the
+    oracle's."""
+    M, N, K = 320, 400, 2048  # 128 blocks per row of a: the one-pass row kernel
+    a = _input(M, K, "bf16", seed=21)
+    b = _input(N, K, "bf16", seed=22)
+    ga, oa = _cfgs("mse", row=True)
+    gb, ob = _cfgs("mse")
+    ca, sa, aa = fos.quantize(a, ga, scales=_poisoned(M, K))
+    (cb,), (sb,), (ab,) = fos.quantize_list([b], gb, scales=[_poisoned(N, K)])
+    out = fos.mm(ca, sa, aa, cb, sb, ab, ga)
+    torch.cuda.synchronize()
+    ha, hb = a.cpu().float().numpy(), b.cpu().float().numpy()
+    ra, tb = oracle.amax_rows(ha), oracle.amax_tensor(hb)
+    oca, osa, _ = oracle.quantize(ha, oa, ra)
+    ocb, osb, _ = oracle.quantize(hb, ob, tb)
+    _same(sa, oracle.swizzle_scales(osa), "a tiled scales")
+    _same(sb, oracle.swizzle_scales(osb), "b tiled scales")
+    _same(ca, oca, "a codes")
+    _same(cb, ocb, "b codes")
+    ref, bound = oracle.mm_reference(oca, osa, ra, ocb, osb, tb, oa)
+    err = np.abs(out.cpu().numpy().astype(np.float64) - ref)
+    assert np.all(err <= bound + 1e-30), float((err / (bound + 1e-30)).max())
